@@ -1,0 +1,100 @@
+"""Seeded synthetic inputs shared by the tests, the smoke check and the bench.
+
+Holds no attention arithmetic: it only draws random numbers and names the
+workload shapes. Both the CUDA path and the CPU oracle consume what it makes.
+
+Recipe (all on the CPU, one ``torch.Generator`` per workload):
+  * Q, K, V are drawn in that order as fp32 N(0, 1) of shape [B, S, H, d];
+  * for the FP8 workload, after each tensor's values a Bernoulli(0.001) mask is
+    drawn from the same generator and the selected entries are multiplied by 20
+    (outliers);
+  * bf16 workloads round the fp32 draw to bf16 (round-to-nearest-even, torch's
+    cast); the FP8 workload hands the fp32 draw to the block quantiser.
+The pages' own benchmark shape is "sequence length 8K, head dim 128"; no public
+dataset is involved.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import numpy as np
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    Hq: int
+    Hkv: int
+    Sq: int
+    Sk: int
+    d: int
+    causal: bool
+    dtype: str = "bf16"          # "bf16" or "e4m3"
+    outlier_frac: float = 0.0
+    seed: int = 1000
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.d)
+
+    def flops(self) -> float:
+        """Metric FLOP count: 4*B*H*Sq*Sk*d, halved for causal."""
+        f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.d
+        return f / 2 if self.causal else f
+
+
+# The five reference workloads (long-context prefill shapes); the seed is
+# 1000 + the workload's position in this list.
+WORKLOADS = {
+    "tiny_b1h1s128d64": Workload("tiny_b1h1s128d64", 1, 1, 1, 128, 128, 64, False, seed=1000),
+    "b4h16s2048d128_causal": Workload("b4h16s2048d128_causal", 4, 16, 16, 2048, 2048, 128, True,
+                                      seed=1001),
+    "b2h32s8192d128_causal": Workload("b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128, True,
+                                      seed=1002),
+    "b2h32s8192d128": Workload("b2h32s8192d128", 2, 32, 32, 8192, 8192, 128, False, seed=1002),
+    "gqa_b1hq32hkv8s16384d128_causal": Workload("gqa_b1hq32hkv8s16384d128_causal", 1, 32, 8,
+                                                16384, 16384, 128, True, seed=1003),
+    "fp8_b4h16s4096d128": Workload("fp8_b4h16s4096d128", 4, 16, 16, 4096, 4096, 128, False,
+                                   dtype="e4m3", outlier_frac=0.001, seed=1004),
+}
+
+
+def draw_qkv_f32(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac=0.0, outlier_mult=20.0):
+    """fp32 CPU tensors q [B,Sq,Hq,d], k/v [B,Sk,Hkv,d], N(0,1) with optional outliers."""
+    g = torch.Generator().manual_seed(int(seed))
+    out = []
+    for shape in ((B, Sq, Hq, d), (B, Sk, Hkv, d), (B, Sk, Hkv, d)):
+        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        if outlier_frac > 0:
+            hit = torch.rand(shape, generator=g) < outlier_frac
+            x = torch.where(hit, x * outlier_mult, x)
+        out.append(x)
+    return tuple(out)
+
+
+def draw_workload_f32(w: Workload):
+    return draw_qkv_f32(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed, w.outlier_frac)
+
+
+def draw_qkv_bf16(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac=0.0):
+    """bf16 CPU tensors (the fp32 draw rounded to bf16)."""
+    return tuple(t.to(torch.bfloat16) for t in
+                 draw_qkv_f32(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac))
+
+
+def bf16_bits(t: torch.Tensor) -> np.ndarray:
+    """Raw uint16 bits of a bf16 CPU tensor, as numpy (for the oracle)."""
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def sample_rows(B, H, Sq, n, seed):
+    """n distinct flat row indices (b*H + h)*Sq + i, always including the first
+    and last row of the first and last (b, h) so edge rows are covered."""
+    total = B * H * Sq
+    g = np.random.default_rng(seed)
+    pick = set(int(x) for x in g.choice(total, size=min(n, total), replace=False))
+    pick.update({0, Sq - 1, total - Sq, total - 1})
+    return np.array(sorted(pick), dtype=np.int64)

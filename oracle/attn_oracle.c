@@ -1,0 +1,246 @@
+/*
+ * attn_oracle.c -- CPU oracle for the exact attention forward pass.
+ *
+ * TEST INFRASTRUCTURE ONLY. Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library. The product path (the
+ * CUDA library under exact_attention_forward_14_b300/) never calls it and
+ * shares no code with it.
+ *
+ * Source of the method: "FlashAttention-3 deep dive: asynchronous TMA and
+ * WGMMA on NVIDIA Hopper H100 ..." (techknowgenie.com/posts/109164421204410442),
+ * referred to below as [FA3]. Sections cited by their heading:
+ *   [FA3 intro]   standard attention materialises the S x S score matrix;
+ *                 FlashAttention computes the same result tile by tile with an
+ *                 online softmax (the method is exact).
+ *   [FA3 s2]      "3-stage asynchronous software pipelining": S = Q K^T,
+ *                 softmax with running max / sum statistics, O = P V.
+ *   [FA3 s4]      "FP8 low-precision arithmetic and numerical stability",
+ *                 sub-section "block quantisation and dynamic scaling":
+ *                 independent scale factors per small tile block, taken from
+ *                 the block's local maximum.
+ *
+ * Because the method is exact, the oracle is the plain definition of the
+ * result, evaluated in fp64 with two passes over the keys of each query row:
+ *
+ *   s_ij  = scale * sum_k q[b,i,hq,k] * k[b,j,hkv,k]      for j in V_i
+ *   m_i   = max_j s_ij                                     (pass 1)
+ *   l_i   = sum_j exp(s_ij - m_i)                          (pass 2)
+ *   O_i   = sum_j exp(s_ij - m_i) * v[b,j,hkv,:] / l_i
+ *   LSE_i = m_i + ln(l_i)
+ *
+ * Readings where the pages are silent (the pages define neither GQA, causal
+ * alignment, the LSE output nor the tensor layouts):
+ *   - layouts: Q, O are [B, Sq, Hq, d]; K, V are [B, Sk, Hkv, d]; LSE is
+ *     [B, Hq, Sq]; all contiguous;
+ *   - GQA: hkv = hq / (Hq / Hkv) (consecutive query heads share a KV head);
+ *   - causal: bottom-right alignment, V_i = { j : j <= i + Sk - Sq };
+ *   - a row with no visible key has O = 0 and LSE = -inf;
+ *   - LSE is the natural logarithm.
+ *
+ * FP8 inputs: element value = decode_e4m3(code) * scale[b, h, row / 64], the
+ * block being 64 consecutive sequence rows of one head times all d columns.
+ * The quantiser that produces these codes follows [FA3 s4]: per block,
+ * s = amax / 448 (s = 1 when amax = 0), code = RNE_saturate_e4m3(x / s); the
+ * division and the amax are evaluated in fp32, the precision in which the
+ * quantised code is decided.
+ *
+ * Build: gcc -O2 -fopenmp -shared -fPIC attn_oracle.c -o liboracle.so -lm
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_DTYPE_BF16 0
+#define ORACLE_DTYPE_E4M3 1
+#define ORACLE_FP8_BLOCK_ROWS 64
+
+/* ---------------------------------------------------------------- codecs -- */
+
+/* bfloat16 is the upper half of an IEEE binary32 value. */
+static double bf16_bits_to_double(uint16_t h) {
+    uint32_t u = ((uint32_t)h) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* OCP 8-bit floating point, E4M3 ("fn" variant): 1 sign bit, 4 exponent bits
+ * with bias 7, 3 mantissa bits; exponent field 0 encodes subnormals
+ * m * 2^-9; the all-ones pattern S.1111.111 is NaN; there is no infinity, so
+ * the largest finite magnitude is 1.110 * 2^8 = 448. */
+double oracle_e4m3_decode(uint8_t c) {
+    int sign = (c >> 7) & 1;
+    int e = (c >> 3) & 0xF;
+    int m = c & 0x7;
+    double mag;
+    if (e == 0xF && m == 0x7) return NAN;
+    if (e == 0) mag = ldexp((double)m, -9);
+    else mag = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Round-to-nearest-even into E4M3 with saturation to +-448 (values beyond the
+ * largest finite magnitude become that magnitude). NaN input gives 0x7F. */
+uint8_t oracle_e4m3_encode(float x) {
+    uint8_t sign = signbit(x) ? 0x80 : 0x00;
+    double a = fabs((double)x);
+    if (isnan(x)) return 0x7F;
+    if (a >= 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        /* subnormal range: a multiple of 2^-9, 0..8 (8 is the smallest normal,
+         * whose code 0x08 follows on from the subnormal codes) */
+        double q = nearbyint(ldexp(a, 9)); /* default rounding: ties to even */
+        return sign | (uint8_t)q;
+    }
+    int e;
+    double fr = frexp(a, &e); /* a = fr * 2^e, fr in [0.5, 1) */
+    int ue = e - 1;            /* a = (2 fr) * 2^ue, 2 fr in [1, 2) */
+    double mant = nearbyint((2.0 * fr - 1.0) * 8.0);
+    if (mant >= 8.0) { mant = 0.0; ue += 1; }
+    int field = ue + 7;
+    if (field > 15 || (field == 15 && mant > 6.0)) return sign | 0x7E;
+    return sign | (uint8_t)((field << 3) | (int)mant);
+}
+
+/* -------------------------------------------------- FP8 block quantiser -- */
+
+/* x: fp32 [B, S, H, d]; codes: u8 [B, S, H, d]; scales: fp32 [B, H, nblk]
+ * with nblk = ceil(S / 64). [FA3 s4] block quantisation. */
+void oracle_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scales,
+                              int B, int S, int H, int d) {
+    int nblk = (S + ORACLE_FP8_BLOCK_ROWS - 1) / ORACLE_FP8_BLOCK_ROWS;
+#pragma omp parallel for collapse(3) schedule(static)
+    for (int b = 0; b < B; ++b)
+        for (int h = 0; h < H; ++h)
+            for (int blk = 0; blk < nblk; ++blk) {
+                int r0 = blk * ORACLE_FP8_BLOCK_ROWS;
+                int r1 = r0 + ORACLE_FP8_BLOCK_ROWS;
+                if (r1 > S) r1 = S;
+                float amax = 0.0f;
+                for (int r = r0; r < r1; ++r) {
+                    const float* row = x + (((size_t)b * S + r) * H + h) * (size_t)d;
+                    for (int c = 0; c < d; ++c) {
+                        float a = fabsf(row[c]);
+                        if (a > amax) amax = a;
+                    }
+                }
+                float s = (amax == 0.0f) ? 1.0f : amax / 448.0f;
+                scales[((size_t)b * H + h) * nblk + blk] = s;
+                for (int r = r0; r < r1; ++r) {
+                    size_t off = (((size_t)b * S + r) * H + h) * (size_t)d;
+                    for (int c = 0; c < d; ++c) {
+                        float t = x[off + c] / s; /* fp32 IEEE division */
+                        codes[off + c] = oracle_e4m3_encode(t);
+                    }
+                }
+            }
+}
+
+/* ------------------------------------------------------------ attention -- */
+
+typedef struct {
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* q_scale;
+    const float* k_scale;
+    const float* v_scale;
+    int dtype;
+    int B, Hq, Hkv, Sq, Sk, d;
+} oracle_inputs;
+
+/* Value of element [b, s, h, c] of a [B, S, H, d] operand, decoded exactly to
+ * fp64. For E4M3 the block scale of (b, h, s/64) multiplies the code. */
+static double load_elem(const oracle_inputs* in, const void* base, const float* scale,
+                        int S, int H, int b, int s, int h, int c) {
+    size_t idx = (((size_t)b * S + s) * H + h) * (size_t)in->d + c;
+    if (in->dtype == ORACLE_DTYPE_BF16) return bf16_bits_to_double(((const uint16_t*)base)[idx]);
+    int nblk = (S + ORACLE_FP8_BLOCK_ROWS - 1) / ORACLE_FP8_BLOCK_ROWS;
+    double sc = (double)scale[((size_t)b * H + h) * nblk + s / ORACLE_FP8_BLOCK_ROWS];
+    return oracle_e4m3_decode(((const uint8_t*)base)[idx]) * sc;
+}
+
+/* One query row (b, hq, i): writes d outputs to o_row and returns LSE.
+ * work: scratch of Sk + 2*d doubles. */
+static double attn_row(const oracle_inputs* in, int causal, double scale, int b, int hq,
+                       int i, double* o_row, double* work) {
+    const int d = in->d;
+    const int group = in->Hq / in->Hkv;
+    const int hkv = hq / group;
+    long jmax = in->Sk - 1; /* last visible key */
+    if (causal) {
+        long lim = (long)i + (long)in->Sk - (long)in->Sq;
+        if (lim < jmax) jmax = lim;
+    }
+    if (jmax < 0) {
+        for (int c = 0; c < d; ++c) o_row[c] = 0.0;
+        return -INFINITY;
+    }
+    double* s = work;          /* Sk scores */
+    double* qrow = work + in->Sk; /* d */
+    double* acc = qrow + d;     /* d */
+    for (int c = 0; c < d; ++c)
+        qrow[c] = load_elem(in, in->q, in->q_scale, in->Sq, in->Hq, b, i, hq, c);
+
+    /* pass 1: scores and their maximum */
+    double m = -INFINITY;
+    for (long j = 0; j <= jmax; ++j) {
+        double dot = 0.0;
+        for (int c = 0; c < d; ++c)
+            dot += qrow[c] * load_elem(in, in->k, in->k_scale, in->Sk, in->Hkv, b, (int)j, hkv, c);
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    /* pass 2: normaliser and weighted sum of values */
+    double l = 0.0;
+    for (int c = 0; c < d; ++c) acc[c] = 0.0;
+    for (long j = 0; j <= jmax; ++j) {
+        double w = exp(s[j] - m);
+        l += w;
+        for (int c = 0; c < d; ++c)
+            acc[c] += w * load_elem(in, in->v, in->v_scale, in->Sk, in->Hkv, b, (int)j, hkv, c);
+    }
+    for (int c = 0; c < d; ++c) o_row[c] = acc[c] / l;
+    return m + log(l);
+}
+
+static int check_dims(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || d <= 0) return 1;
+    if (Hq % Hkv != 0) return 1;
+    return 0;
+}
+
+/* Full evaluation. o: fp64 [B, Sq, Hq, d]; lse: fp64 [B, Hq, Sq].
+ * If rows != NULL, only the nrows listed rows are evaluated: rows[r] is the
+ * flat index (b * Hq + hq) * Sq + i, o receives nrows x d values and lse
+ * nrows values, in list order. Returns 0, or 1 on bad dimensions. */
+int oracle_attn_fwd(const void* q, const void* k, const void* v,
+                    const float* q_scale, const float* k_scale, const float* v_scale,
+                    int dtype, double* o, double* lse,
+                    int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal, double scale,
+                    const int64_t* rows, int64_t nrows) {
+    if (check_dims(B, Hq, Hkv, Sq, Sk, d)) return 1;
+    if (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_E4M3) return 1;
+    if (dtype == ORACLE_DTYPE_E4M3 && (!q_scale || !k_scale || !v_scale)) return 1;
+    oracle_inputs in = {q, k, v, q_scale, k_scale, v_scale, dtype, B, Hq, Hkv, Sq, Sk, d};
+    int64_t total = rows ? nrows : (int64_t)B * Hq * Sq;
+#pragma omp parallel
+    {
+        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+#pragma omp for schedule(dynamic, 4)
+        for (int64_t r = 0; r < total; ++r) {
+            int64_t flat = rows ? rows[r] : r;
+            int i = (int)(flat % Sq);
+            int64_t bh = flat / Sq;
+            int hq = (int)(bh % Hq);
+            int b = (int)(bh / Hq);
+            double* o_row = rows ? o + (size_t)r * d
+                                 : o + (((size_t)b * Sq + i) * Hq + hq) * (size_t)d;
+            double val = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+            lse[rows ? r : flat] = val;
+        }
+        free(work);
+    }
+    return 0;
+}

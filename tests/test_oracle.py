@@ -1,0 +1,302 @@
+"""Pins for the CPU oracle, checked against things other than itself:
+hand-worked cases, closed forms, invariants, brute force on tiny inputs and
+library routines. CPU only."""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from exact_attention_forward_14_b300 import inputs
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def bf16(x):
+    """Round an array to bf16 and return (uint16 bits, float64 values)."""
+    t = torch.as_tensor(np.asarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return inputs.bf16_bits(t), t.to(torch.float64).numpy()
+
+
+def rand_case(rng, B, Hq, Hkv, Sq, Sk, d, scale_mag=1.0):
+    q = rng.standard_normal((B, Sq, Hq, d)) * scale_mag
+    k = rng.standard_normal((B, Sk, Hkv, d)) * scale_mag
+    v = rng.standard_normal((B, Sk, Hkv, d))
+    return bf16(q), bf16(k), bf16(v)
+
+
+def brute_force(q, k, v, causal, scale):
+    """Materialised softmax in plain Python floats: exp of the raw scores (no
+    max subtraction, inputs are tiny), normalised after the fact."""
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    g = Hq // Hkv
+    o = np.zeros((B, Sq, Hq, d))
+    lse = np.zeros((B, Hq, Sq))
+    for b in range(B):
+        for h in range(Hq):
+            hk = h // g
+            for i in range(Sq):
+                weights = []
+                for j in range(Sk):
+                    if causal and j > i + Sk - Sq:
+                        weights.append(0.0)
+                        continue
+                    s = sum(float(q[b, i, h, c]) * float(k[b, j, hk, c]) for c in range(d))
+                    weights.append(math.exp(scale * s))
+                z = sum(weights)
+                if z == 0.0:
+                    lse[b, h, i] = -math.inf
+                    continue
+                lse[b, h, i] = math.log(z)
+                for c in range(d):
+                    o[b, i, h, c] = sum(weights[j] * float(v[b, j, hk, c]) for j in range(Sk)) / z
+    return o, lse
+
+
+def test_hand_worked_golden(oracle_mod):
+    with open(os.path.join(GOLDEN, "hand_worked_attention.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        shp_q = (c["B"], c["Sq"], c["Hq"], c["d"])
+        shp_k = (c["B"], c["Sk"], c["Hkv"], c["d"])
+        (qb, _), (kb, _), (vb, _) = (bf16(np.reshape(c["q"], shp_q)),
+                                     bf16(np.reshape(c["k"], shp_k)),
+                                     bf16(np.reshape(c["v"], shp_k)))
+        o, lse = oracle_mod.attn_fwd(qb, kb, vb, c["causal"], c["scale"])
+        np.testing.assert_allclose(o.ravel(), c["o"], rtol=0, atol=1e-12, err_msg=c["name"])
+        want = np.array([-np.inf if x is None else x for x in c["lse"]])
+        np.testing.assert_allclose(lse.ravel(), want, rtol=0, atol=1e-12, err_msg=c["name"])
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", [(1, 1, 1, 1, 1, 1), (1, 2, 1, 3, 5, 2), (2, 4, 2, 8, 8, 4),
+                                   (1, 3, 3, 7, 4, 3), (2, 2, 1, 4, 7, 4)])
+def test_brute_force_tiny(oracle_mod, shape, causal):
+    B, Hq, Hkv, Sq, Sk, d = shape
+    rng = np.random.default_rng(7 + sum(shape))
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, B, Hq, Hkv, Sq, Sk, d)
+    scale = 0.7
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, causal, scale)
+    o_ref, lse_ref = brute_force(q, k, v, causal, scale)
+    np.testing.assert_allclose(o, o_ref, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_single_key_gives_value_and_score(oracle_mod):
+    rng = np.random.default_rng(1)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 2, 4, 2, 5, 1, 8)
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, False, 0.3)
+    for h in range(4):
+        np.testing.assert_array_equal(o[:, :, h, :], v[:, 0:1, h // 2, :].repeat(5, axis=1))
+        s = 0.3 * np.einsum("bid,bd->bi", q[:, :, h, :], k[:, 0, h // 2, :])
+        np.testing.assert_allclose(lse[:, h, :], s, rtol=0, atol=1e-13)
+
+
+def test_causal_first_row_is_first_value(oracle_mod):
+    rng = np.random.default_rng(2)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 1, 2, 2, 33, 33, 16, scale_mag=3.0)
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, True, 0.25)
+    np.testing.assert_array_equal(o[:, 0], v[:, 0])
+    np.testing.assert_allclose(lse[:, :, 0], 0.25 * np.einsum("bhd,bhd->bh", q[:, 0], k[:, 0]),
+                               rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_identical_keys_give_mean_of_visible_values(oracle_mod, causal):
+    rng = np.random.default_rng(3)
+    Sq, Sk, d = 6, 9, 8
+    (qb, q), _, (vb, v) = rand_case(rng, 1, 1, 1, Sq, Sk, d)
+    krow = rng.standard_normal(d)
+    kb, k = bf16(np.broadcast_to(krow, (1, Sk, 1, d)))
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, causal, 0.5)
+    for i in range(Sq):
+        n = min(Sk, i + Sk - Sq + 1) if causal else Sk
+        np.testing.assert_allclose(o[0, i, 0], v[0, :n, 0].mean(axis=0), rtol=0, atol=1e-13)
+        s = 0.5 * float(q[0, i, 0] @ k[0, 0, 0])
+        np.testing.assert_allclose(lse[0, 0, i], s + math.log(n), rtol=0, atol=1e-13)
+
+
+def test_zero_query_gives_uniform_weights(oracle_mod):
+    rng = np.random.default_rng(4)
+    _, (kb, k), (vb, v) = rand_case(rng, 1, 1, 1, 4, 11, 8)
+    qb, _ = bf16(np.zeros((1, 4, 1, 8)))
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, False, 1.0)
+    np.testing.assert_allclose(o[0, :, 0], np.broadcast_to(v[0, :, 0].mean(0), (4, 8)), atol=1e-13)
+    np.testing.assert_allclose(lse, math.log(11), atol=1e-13)
+
+
+def test_joint_permutation_of_keys_and_values(oracle_mod):
+    rng = np.random.default_rng(5)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 2, 2, 1, 7, 19, 8)
+    perm = rng.permutation(19)
+    o1, l1 = oracle_mod.attn_fwd(qb, kb, vb, False, 0.4)
+    o2, l2 = oracle_mod.attn_fwd(qb, kb[:, perm], vb[:, perm], False, 0.4)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+    # ...and a permutation of K alone changes the result (the pin can fail).
+    o3, _ = oracle_mod.attn_fwd(qb, kb[:, perm], vb, False, 0.4)
+    assert np.abs(o3 - o1).max() > 1e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gqa_equals_mha_on_duplicated_kv_heads(oracle_mod, causal):
+    rng = np.random.default_rng(6)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 2, 8, 2, 10, 12, 8)
+    o1, l1 = oracle_mod.attn_fwd(qb, kb, vb, causal, 0.35)
+    kdup = np.repeat(kb, 4, axis=2)  # head h of the copy = KV head h // 4
+    vdup = np.repeat(vb, 4, axis=2)
+    o2, l2 = oracle_mod.attn_fwd(qb, kdup, vdup, causal, 0.35)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(l1, l2)
+
+
+def test_scaling_q_equals_scaling_scale(oracle_mod):
+    rng = np.random.default_rng(8)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 1, 2, 2, 9, 9, 8)
+    q2b, _ = bf16(q * 2.0)  # power of two: exact in bf16
+    o1, l1 = oracle_mod.attn_fwd(qb, kb, vb, True, 0.6)
+    o2, l2 = oracle_mod.attn_fwd(q2b, kb, vb, True, 0.3)
+    np.testing.assert_allclose(o1, o2, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("sq_sk", [(33, 33), (17, 40), (40, 17)])
+def test_matches_torch_sdpa_fp64(oracle_mod, causal, sq_sk):
+    """Library cross-check: torch's scaled_dot_product_attention in fp64 on the
+    CPU, with an explicit bottom-right causal mask, plus torch.logsumexp."""
+    Sq, Sk = sq_sk
+    rng = np.random.default_rng(9)
+    (qb, q), (kb, k), (vb, v) = rand_case(rng, 2, 4, 2, Sq, Sk, 16)
+    scale = 1 / 4
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, causal, scale)
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(np.repeat(k, 2, axis=2)).permute(0, 2, 1, 3)
+    tv = torch.from_numpy(np.repeat(v, 2, axis=2)).permute(0, 2, 1, 3)
+    i = torch.arange(Sq)[:, None]
+    j = torch.arange(Sk)[None, :]
+    mask = (j <= i + Sk - Sq) if causal else torch.ones(Sq, Sk, dtype=torch.bool)
+    scores = (tq @ tk.transpose(-1, -2)) * scale
+    scores = scores.masked_fill(~mask, -math.inf)
+    ref_lse = torch.logsumexp(scores, dim=-1)
+    visible = mask.any(dim=-1)
+    ref_o = torch.nn.functional.scaled_dot_product_attention(
+        tq, tk, tv, attn_mask=mask | ~visible[:, None], scale=scale)
+    ref_o = ref_o.masked_fill(~visible[None, None, :, None], 0.0).permute(0, 2, 1, 3)
+    np.testing.assert_allclose(o, ref_o.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_lse.numpy(), rtol=0, atol=1e-12)
+
+
+def test_row_subset_matches_full(oracle_mod):
+    rng = np.random.default_rng(10)
+    (qb, _), (kb, _), (vb, _) = rand_case(rng, 2, 4, 2, 21, 21, 8)
+    o, lse = oracle_mod.attn_fwd(qb, kb, vb, True, 0.5)
+    rows = inputs.sample_rows(2, 4, 21, 25, seed=0)
+    o_s, lse_s = oracle_mod.attn_fwd(qb, kb, vb, True, 0.5, rows=rows)
+    b, rem = np.divmod(rows, 4 * 21)
+    h, i = np.divmod(rem, 21)
+    np.testing.assert_array_equal(o_s, o[b, i, h])
+    np.testing.assert_array_equal(lse_s, lse[b, h, i])
+
+
+# ------------------------------------------------------------- E4M3 codec --
+
+def test_e4m3_decode_known_codes(oracle_mod):
+    table = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0,
+             0x3C: 1.5, 0x40: 2.0, 0x7E: 448.0, 0xFE: -448.0, 0xB8: -1.0, 0x80: -0.0}
+    got = oracle_mod.e4m3_decode(np.array(list(table), dtype=np.uint8))
+    np.testing.assert_array_equal(got, np.array(list(table.values())))
+    assert np.isnan(oracle_mod.e4m3_decode(np.array([0x7F, 0xFF], dtype=np.uint8))).all()
+
+
+def test_e4m3_decode_matches_torch(oracle_mod):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle_mod.e4m3_decode(codes), ref)
+
+
+def _nearest_even_brute(x):
+    """Nearest finite E4M3 value by exhaustive search; ties to the even code."""
+    codes = [c for c in range(256) if c not in (0x7F, 0xFF)]
+    vals = {c: (-1.0 if c & 0x80 else 1.0) * (
+        (c & 7) * 2.0 ** -9 if (c >> 3) & 15 == 0 else (1 + (c & 7) / 8) * 2.0 ** (((c >> 3) & 15) - 7))
+        for c in codes}
+    if abs(x) >= 448:
+        return 0x7E | (0x80 if x < 0 else 0)
+    best = min(codes, key=lambda c: (abs(vals[c] - x), c & 1, -(c & 0x80 == (0x80 if x < 0 else 0))))
+    return best
+
+
+def test_e4m3_encode_matches_brute_force_and_torch(oracle_mod):
+    rng = np.random.default_rng(11)
+    finite = oracle_mod.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = (finite[1:] + finite[:-1]) / 2  # exact ties (all representable in fp32)
+    x = np.concatenate([finite, mids, -mids, rng.standard_normal(2000) * 40,
+                        rng.standard_normal(500) * 0.01, [0.0, 447.9, 448.0, 460.0, 470.0, 1e6]])
+    x = x.astype(np.float32)
+    got = oracle_mod.e4m3_encode(x)
+    brute = np.array([_nearest_even_brute(float(v)) for v in x], dtype=np.uint8)
+    # compare values (the sign of zero aside)
+    np.testing.assert_array_equal(oracle_mod.e4m3_decode(got), oracle_mod.e4m3_decode(brute))
+    inrange = np.abs(x) <= 448
+    ref = torch.from_numpy(x[inrange]).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(got[inrange], ref)
+    assert oracle_mod.e4m3_decode(got[~inrange]).tolist() == [448.0] * int((~inrange).sum())
+
+
+# -------------------------------------------------------- FP8 quantiser --
+
+def test_quantiser_block_scales_and_codes(oracle_mod):
+    rng = np.random.default_rng(12)
+    B, S, H, d = 2, 150, 3, 16  # 3 blocks of 64 rows, the last one ragged (22 rows)
+    x = rng.standard_normal((B, S, H, d)).astype(np.float32)
+    x[1, 64:128, 2, :] = 0.0  # an all-zero block
+    codes, scales = oracle_mod.quantize_fp8_e4m3(x)
+    assert scales.shape == (B, H, 3)
+    for b in range(B):
+        for h in range(H):
+            for blk in range(3):
+                xs = x[b, blk * 64:(blk + 1) * 64, h, :]
+                amax = np.float32(np.abs(xs).max())
+                s = np.float32(1.0) if amax == 0 else np.float32(amax / np.float32(448.0))
+                assert scales[b, h, blk] == s
+                cs = codes[b, blk * 64:(blk + 1) * 64, h, :]
+                if amax == 0:
+                    assert (cs == 0).all()
+                    continue
+                # the block maximum lands on the largest code (|x|/s rounds to 448)
+                at = np.unravel_index(np.abs(xs).argmax(), xs.shape)
+                assert cs[at] & 0x7F == 0x7E
+                deq = oracle_mod.e4m3_decode(cs) * float(s)
+                err = np.abs(deq - xs)
+                # half a unit in the last place: 2^-4 relative for normals,
+                # 2^-10 * s absolute in the subnormal range
+                bound = np.maximum(np.abs(xs) * 2.0 ** -4, 2.0 ** -10 * float(s))
+                assert (err <= bound * (1 + 1e-6)).all()
+
+
+def test_fp8_attention_equals_bf16_attention_on_dequantised_values(oracle_mod):
+    """With power-of-two block scales, every dequantised value is exact in
+    bf16, so the E4M3 input path must agree with the bf16 input path."""
+    rng = np.random.default_rng(13)
+    B, H, S, d = 1, 2, 130, 8
+    nblk = 3
+    codes = [rng.integers(0, 0x7E, size=(B, S, H, d), dtype=np.uint8) |
+             (rng.integers(0, 2, size=(B, S, H, d), dtype=np.uint8) << 7) for _ in range(3)]
+    scales = [np.exp2(rng.integers(-4, 3, size=(B, H, nblk))).astype(np.float32) for _ in range(3)]
+    deq = []
+    for c, s in zip(codes, scales):
+        rows_blk = np.arange(S) // 64
+        val = oracle_mod.e4m3_decode(c) * s[:, :, rows_blk].transpose(0, 2, 1)[..., None]
+        deq.append(bf16(val))
+    for causal in (False, True):
+        o8, l8 = oracle_mod.attn_fwd(*codes, causal, 0.2, dtype="e4m3", q_scale=scales[0],
+                                     k_scale=scales[1], v_scale=scales[2])
+        o16, l16 = oracle_mod.attn_fwd(deq[0][0], deq[1][0], deq[2][0], causal, 0.2)
+        np.testing.assert_array_equal(deq[0][1], oracle_mod.e4m3_decode(codes[0]) *
+                                      scales[0][:, :, np.arange(S) // 64].transpose(0, 2, 1)[..., None])
+        np.testing.assert_allclose(o8, o16, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(l8, l16, rtol=0, atol=1e-12)
