@@ -1,0 +1,180 @@
+"""Exact attention forward for B300 (sm_103a): Python binding of libattn_b300.
+
+The functions named like the C ABI (``attn_fwd``, ``attn_fwd_fp8``,
+``attn_quantize_fp8_e4m3``, ``attn_device_status``, ``attn_status_string``)
+only marshal arguments: tensors become device pointers, a torch stream (or
+None = torch's current stream) becomes a cudaStream_t; they return the C
+status code. ``forward``, ``forward_fp8`` and ``quantize_fp8`` additionally
+allocate the outputs with torch and raise ``AttnError`` on a non-zero status.
+All compute runs in the CUDA library; there is no fallback path: if the
+library is missing every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+__all__ = [
+    "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
+    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError",
+    "attn_fwd", "attn_fwd_fp8", "attn_quantize_fp8_e4m3", "attn_device_status",
+    "attn_status_string", "forward", "forward_fp8", "quantize_fp8", "library_path", "load",
+]
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_MISALIGNED = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_TIMEOUT = 5
+ATTN_BF16 = 0
+ATTN_FP8_E4M3 = 1
+FP8_BLOCK_ROWS = 64
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "libattn_b300.so")
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, what: str = ""):
+        self.code = code
+        super().__init__(f"{what}: {attn_status_string(code)} ({code})" if what else
+                         f"{attn_status_string(code)} ({code})")
+
+
+def load():
+    """Load libattn_b300.so (built in-tree by ``exact_attention_forward_14_b300.build``)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: build it with `python -m exact_attention_forward_14_b300.build`"
+                " (nvcc, sm_103a); this package has no non-CUDA fallback")
+        lib = ctypes.CDLL(path)
+        P, I, F = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+        lib.attn_fwd.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, P]
+        lib.attn_fwd.restype = I
+        lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
+        lib.attn_fwd_fp8.restype = I
+        lib.attn_quantize_fp8_e4m3.argtypes = [P, P, P, I, I, I, I, P]
+        lib.attn_quantize_fp8_e4m3.restype = I
+        lib.attn_device_status.argtypes = [P]
+        lib.attn_device_status.restype = I
+        lib.attn_status_string.argtypes = [I]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _ptr(x):
+    """Device pointer of a tensor, or an int passed through (0 / None = NULL)."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x or None
+    return x.data_ptr() or None
+
+
+def _stream(s):
+    if s is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream or None
+    if isinstance(s, int):
+        return s or None
+    return s.cuda_stream or None
+
+
+# ----------------------------------------------------------- C ABI mirror --
+
+def attn_fwd(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype=ATTN_BF16,
+             stream=None) -> int:
+    return load().attn_fwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B), int(Hq),
+                           int(Hkv), int(Sq), int(Sk), int(d), int(bool(causal)), float(scale),
+                           int(dtype), _stream(stream))
+
+
+def attn_fwd_fp8(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+                 scale, stream=None) -> int:
+    return load().attn_fwd_fp8(_ptr(q), _ptr(k), _ptr(v), _ptr(q_scale), _ptr(k_scale),
+                               _ptr(v_scale), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
+                               int(Sq), int(Sk), int(d), int(bool(causal)), float(scale),
+                               _stream(stream))
+
+
+def attn_quantize_fp8_e4m3(x, codes, scale, B, S, H, d, stream=None) -> int:
+    return load().attn_quantize_fp8_e4m3(_ptr(x), _ptr(codes), _ptr(scale), int(B), int(S),
+                                         int(H), int(d), _stream(stream))
+
+
+def attn_device_status(stream=None) -> int:
+    return load().attn_device_status(_stream(stream))
+
+
+def attn_status_string(code: int) -> str:
+    return load().attn_status_string(int(code)).decode()
+
+
+# ------------------------------------------------------ tensor conveniences --
+
+def _check(rc, what):
+    if rc != ATTN_OK:
+        raise AttnError(rc, what)
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+            stream=None):
+    """bf16 attention forward. q [B,Sq,Hq,d], k/v [B,Sk,Hkv,d] (CUDA, contiguous).
+    Returns (o bf16 [B,Sq,Hq,d], lse fp32 [B,Hq,Sq])."""
+    import torch
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    for t in (q, k, v, out, lse):
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    _check(attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, ATTN_BF16, stream),
+           "attn_fwd")
+    return out, lse
+
+
+def forward_fp8(q, k, v, q_scale, k_scale, v_scale, causal: bool = False,
+                scale: float | None = None, out=None, lse=None, stream=None):
+    """E4M3 attention forward with per-64-row block scales. Returns (o bf16, lse fp32)."""
+    import torch
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(attn_fwd_fp8(q, k, v, q_scale, k_scale, v_scale, out, lse, B, Hq, Hkv, Sq, Sk, d,
+                        causal, scale, stream), "attn_fwd_fp8")
+    return out, lse
+
+
+def quantize_fp8(x, stream=None):
+    """fp32 x [B,S,H,d] (CUDA) -> (E4M3 codes as uint8 [B,S,H,d], fp32 scales [B,H,ceil(S/64)])."""
+    import torch
+    B, S, H, d = x.shape
+    codes = torch.empty((B, S, H, d), dtype=torch.uint8, device=x.device)
+    scales = torch.empty((B, H, (S + FP8_BLOCK_ROWS - 1) // FP8_BLOCK_ROWS), dtype=torch.float32,
+                         device=x.device)
+    _check(attn_quantize_fp8_e4m3(x, codes, scales, B, S, H, d, stream), "attn_quantize_fp8_e4m3")
+    return codes, scales

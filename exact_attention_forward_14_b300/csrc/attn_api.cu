@@ -1,0 +1,237 @@
+// attn_api.cu -- host side of libattn_b300.so: argument validation, TMA
+// tensor-map encoding, launch of the fused attention kernel and of the FP8
+// block quantiser, and the device status word.
+//
+// The C ABI is declared (with argument meaning, layouts, ownership and error
+// behaviour) in include/attn_b300.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "attn_b300.h"
+#include "attn_fwd_kernel.cuh"
+#include "quantize_fp8.cuh"
+#include "tmap.cuh"
+
+namespace {
+
+using attnb3::Cfg;
+using attnb3::FwdParams;
+using attnb3::encode_bshd;
+using attnb3::get_encoder;
+
+// Device status word written by the kernels' watchdog (ATTN_ERR_TIMEOUT).
+__device__ int g_attn_status = 0;
+
+constexpr int kMaxDevices = 64;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+
+struct DeviceInfo {
+  std::once_flag once;
+  int ok = 0;  // 1 = usable sm_103 device
+  int num_sms = 0;
+  int* status = nullptr;
+  std::atomic<uint32_t> attr_done{0};  // bit per kernel instantiation
+};
+DeviceInfo g_dev[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Checks on the current device, done once per device.
+int current_device(DeviceInfo** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  DeviceInfo& di = g_dev[dev];
+  std::call_once(di.once, [&] {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      di.ok = -1;
+      return;
+    }
+    if (major != 10 || minor != 3) {
+      di.ok = 0;
+      return;
+    }
+    void* st = nullptr;
+    if (cudaGetSymbolAddress(&st, g_attn_status) != cudaSuccess) {
+      di.ok = -1;
+      return;
+    }
+    di.status = static_cast<int*>(st);
+    di.num_sms = sms;
+    di.ok = 1;
+  });
+  if (di.ok < 0) return ATTN_ERR_CUDA;
+  if (di.ok == 0) return ATTN_ERR_UNSUPPORTED;
+  *out = &di;
+  return ATTN_OK;
+}
+
+bool fits_i32(long long a, long long b, long long c, long long d) {
+  const long long lim = 0x7fffffffLL;
+  long long x = a;
+  for (long long f : {b, c, d}) {
+    if (x > lim / f) return false;
+    x *= f;
+  }
+  return x <= lim;
+}
+
+template <int D, bool FP8>
+int launch(const void* q, const void* k, const void* v, const float* qs, const float* ks,
+           const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk,
+           int causal, float scale, cudaStream_t stream, DeviceInfo* di, uint32_t attr_bit) {
+  using C = Cfg<D, FP8>;
+  auto kern = attnb3::attn_fwd_kernel<D, FP8>;
+  if (!(di->attr_done.load(std::memory_order_acquire) & attr_bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
+  }
+  CUtensorMap tq, tk, tv;
+  if (!encode_bshd(&tq, q, FP8, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BM) ||
+      !encode_bshd(&tk, k, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN) ||
+      !encode_bshd(&tv, v, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN))
+    return ATTN_ERR_CUDA;
+
+  FwdParams P;
+  P.o = static_cast<__nv_bfloat16*>(o);
+  P.lse = lse;
+  P.q_scale = qs;
+  P.k_scale = ks;
+  P.v_scale = vs;
+  P.B = B;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.Sq = Sq;
+  P.Sk = Sk;
+  P.group = Hq / Hkv;
+  P.n_qp = (Sq + attnb3::UNIT_ROWS - 1) / attnb3::UNIT_ROWS;
+  P.nkv = (Sk + attnb3::BN - 1) / attnb3::BN;
+  P.num_units = B * Hq * P.n_qp;
+  P.causal = causal ? 1 : 0;
+  P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  P.timeout_ns = kWaitLimitNs;
+  P.status = di->status;
+
+  const int grid = P.num_units < di->num_sms ? P.num_units : di->num_sms;
+  kern<<<grid, attnb3::NUM_THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+// Argument checks shared by both attention entry points (no CUDA calls).
+int check_attn_args(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                    int Hq, int Hkv, int Sq, int Sk, int d, float scale) {
+  if (!q || !k || !v || !o || !lse) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
+  if (!fits_i32(B, Sq, Hq, d) || !fits_i32(B, Sk, Hkv, d)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
+    return ATTN_ERR_MISALIGNED;
+  return ATTN_OK;
+}
+
+int run_attn(const void* q, const void* k, const void* v, const float* qs, const float* ks,
+             const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
+             int causal, float scale, bool fp8, cudaStream_t stream) {
+  DeviceInfo* di = nullptr;
+  int rc = current_device(&di);
+  if (rc != ATTN_OK) return rc;
+  if (!get_encoder()) return ATTN_ERR_CUDA;
+  if (!fp8 && d == 128)
+    return launch<128, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                              stream, di, 1u);
+  if (!fp8 && d == 64)
+    return launch<64, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                             stream, di, 2u);
+  if (fp8 && d == 128)
+    return launch<128, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                             stream, di, 4u);
+  if (fp8 && d == 64)
+    return launch<64, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
+                            stream, di, 8u);
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" {
+
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+             int Hkv, int Sq, int Sk, int d, int causal, float scale, int dtype,
+             attn_stream_t stream) {
+  int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (dtype == ATTN_BF16)
+    return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+                    scale, false, reinterpret_cast<cudaStream_t>(stream));
+  if (dtype == ATTN_FP8_E4M3)  // null scale pointers: every block scale is 1
+    return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+                    scale, true, reinterpret_cast<cudaStream_t>(stream));
+  return ATTN_ERR_UNSUPPORTED;
+}
+
+int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_scale,
+                 const float* k_scale, const float* v_scale, void* o, float* lse, int B, int Hq,
+                 int Hkv, int Sq, int Sk, int d, int causal, float scale, attn_stream_t stream) {
+  int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return ATTN_ERR_MISALIGNED;
+  return run_attn(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
+                  scale, true, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, int S, int H,
+                           int d, attn_stream_t stream) {
+  if (!x || !codes || !scale) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || S <= 0 || H <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!fits_i32(B, S, H, d)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scale, 4)) return ATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  int rc = current_device(&di);
+  if (rc != ATTN_OK) return rc;
+  const int nblk = (S + attnb3::FP8_BLOCK - 1) / attnb3::FP8_BLOCK;
+  const long long ctas = static_cast<long long>(B) * H * nblk;
+  if (ctas > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  attnb3::quantize_fp8_kernel<<<static_cast<unsigned>(ctas), attnb3::QUANT_THREADS, 0,
+                                reinterpret_cast<cudaStream_t>(stream)>>>(x, codes, scale, S, H,
+                                                                          d, nblk);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_device_status(attn_stream_t stream) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpyFromSymbol(&v, g_attn_status, sizeof(int)) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0 && cudaMemcpyToSymbol(g_attn_status, &zero, sizeof(int)) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return v;
+}
+
+const char* attn_status_string(int code) {
+  switch (code) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_MISALIGNED: return "ATTN_ERR_MISALIGNED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    default: return "ATTN_ERR_UNKNOWN";
+  }
+}
+
+}  // extern "C"

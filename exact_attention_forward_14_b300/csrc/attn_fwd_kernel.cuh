@@ -1,0 +1,616 @@
+// attn_fwd_kernel.cuh -- fused exact attention forward for sm_103a (B300).
+//
+// Method: "FlashAttention-3 deep dive: asynchronous TMA and WGMMA on NVIDIA
+// Hopper H100" (techknowgenie.com/posts/109164421204410442), cited as [FA3]:
+//   [FA3 intro]  IO-aware tiling + online softmax: the Sq x Sk score matrix
+//                stays on chip; work is split over query-row tiles;
+//   [FA3 s1]     TMA: one thread issues a bulk tensor copy, completion is
+//                tracked by an mbarrier (producer/consumer hand-off);
+//   [FA3 s2]     three overlapped stages: TMA load of the next K/V tile,
+//                S = Q K^T on the tensor cores, softmax + O += P V for the
+//                previous tile; multi-stage K/V buffers;
+//   [FA3 s3]     the softmax (exp on the MUFU) is the bottleneck the
+//                pipeline must hide; fewer rescales help;
+//   [FA3 s4]     FP8: per-block scale factors, FP8 products with fp32
+//                accumulation, base-2 exponentials.
+// The Hopper specifics there (WGMMA register accumulators, warpgroup-wide
+// MMA) are replaced by the Blackwell forms: tcgen05.mma issued by one thread,
+// fp32 accumulators in tensor memory (TMEM), P handed to the second MMA
+// straight from TMEM.
+//
+// CTA organisation (one persistent CTA per SM, 320 threads):
+//   warps 0-3  softmax for Q tile 0 (thread = one query row = one TMEM lane)
+//   warps 4-7  softmax for Q tile 1 (ping-pong partner of tile 0)
+//   warp  8    MMA issuer (lane 0) and TMEM owner
+//   warp  9    TMA producer (lane 0)
+// A work unit is (b, hq, 256 query rows) = two 128-row Q tiles that share one
+// stream of 128-key K/V tiles. Per K/V tile j the MMA warp issues, in order,
+//   O0 += P0(j) V(j);  S0(j+1) = Q0 K(j+1)^T;  O1 += P1(j) V(j);  S1(j+1) = ...
+// so while softmax 0 works on S0(j+1) the tensor cores run tile 1's MMAs and
+// vice versa. P(j) overwrites the low columns of S(j) in TMEM (bf16 pairs or
+// E4M3 quads per 32-bit column); in-order execution of MMAs from one thread
+// makes S(j+1) wait for P(j)'s consumer.
+//
+// TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+d)
+// O1 [256+d, 256+2d).
+//
+// Online softmax (exact): running max m (log2 units) and sum l per row. The
+// max used for the exponent is only raised when the tile max exceeds it by
+// more than RESCALE_LOG2 (then O and l are rescaled by 2^(m_old - m_new));
+// otherwise p = 2^(s*c - m) <= 2^RESCALE_LOG2. O and l share the stale max,
+// so O / l is unchanged.
+//
+// Every mbarrier wait is bounded by a wall-clock limit; on expiry the CTA
+// records ATTN_ERR_TIMEOUT in the device status word, every role leaves its
+// loop, outstanding copies and MMAs are drained (again with a limit) and the
+// tensor memory is released.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace attnb3 {
+
+constexpr int BM = 128;           // query rows per Q tile
+constexpr int BN = 128;           // keys per K/V tile
+constexpr int UNIT_ROWS = 2 * BM; // query rows per work unit
+constexpr int NUM_THREADS = 320;
+constexpr int WARP_MMA = 8;
+constexpr int WARP_LOAD = 9;
+constexpr float RESCALE_LOG2 = 8.0f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr int STATUS_TIMEOUT = 5;  // ATTN_ERR_TIMEOUT
+constexpr int FP8_BLOCK = 64;      // rows per FP8 scale block
+
+struct FwdParams {
+  __nv_bfloat16* o;
+  float* lse;
+  const float* q_scale;  // FP8 only: [B, Hq, ceil(Sq/64)]
+  const float* k_scale;  // FP8 only: [B, Hkv, ceil(Sk/64)]
+  const float* v_scale;  // FP8 only: [B, Hkv, ceil(Sk/64)]
+  int B, Hq, Hkv, Sq, Sk;
+  int group;      // Hq / Hkv
+  int n_qp;       // ceil(Sq / UNIT_ROWS)
+  int nkv;        // ceil(Sk / BN)
+  int num_units;  // B * Hq * n_qp
+  int causal;
+  float scale_log2;  // softmax scale * log2(e)
+  unsigned long long timeout_ns;
+  int* status;       // device status word
+};
+
+template <int D, bool FP8>
+struct Cfg {
+  static constexpr int ESZ = FP8 ? 1 : 2;
+  static constexpr int ROW_BYTES = D * ESZ;
+  static constexpr int CHUNK_BYTES = ROW_BYTES < 128 ? ROW_BYTES : 128;  // swizzle span
+  static constexpr int CHUNK_ELEMS = CHUNK_BYTES / ESZ;
+  static constexpr int NCHUNK = ROW_BYTES / CHUNK_BYTES;
+  static constexpr uint32_t SWZ_CODE = CHUNK_BYTES == 128 ? 2u : 4u;
+  static constexpr int Q_TILE_BYTES = BM * ROW_BYTES;
+  static constexpr int KV_TILE_BYTES = BN * ROW_BYTES;
+  static constexpr int Q_CHUNK_BYTES = BM * CHUNK_BYTES;
+  static constexpr int KV_CHUNK_BYTES = BN * CHUNK_BYTES;
+  static constexpr int NSLOT = KV_TILE_BYTES >= 32768 ? 4 : 8;
+  static constexpr int MMA_K = FP8 ? 32 : 16;  // 32 bytes of K per instruction
+  static constexpr int KSTEPS_QK = D / MMA_K;
+  static constexpr int KSTEPS_PV = BN / MMA_K;
+  static constexpr int P_COLS = BN * ESZ / 4;  // TMEM columns holding P
+  static constexpr int P_COLS_PER_KSTEP = MMA_K * ESZ / 4;
+  static constexpr uint32_t AB_FMT = FP8 ? 0u : 1u;  // e4m3 : bf16
+  static constexpr uint32_t IDESC_S = make_idesc(BM, BN, AB_FMT, false);
+  static constexpr uint32_t IDESC_PV = make_idesc(BM, D, AB_FMT, true);
+  static constexpr int COL_S0 = 0;
+  static constexpr int COL_O0 = 2 * BN;
+  static constexpr int TMEM_COLS = 512;
+  // shared memory (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = 2 * Q_TILE_BYTES;
+  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_TILE_BYTES;
+  // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
+  // p_full[2], o_full[2], drain
+  static constexpr int NUM_BARS = 2 + 2 * NSLOT + 7;
+  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // Launch with the whole opt-in budget (one CTA per SM either way), so a
+  // descriptor stepping past its tile still reads inside this CTA's window.
+  static constexpr int SMEM_ALLOC = 227 * 1024;
+  static_assert(2 * BN + 2 * D <= TMEM_COLS, "TMEM budget");
+  static_assert(SMEM_BYTES <= SMEM_ALLOC, "shared memory budget");
+  static_assert(D % MMA_K == 0 && D % 32 == 0, "head dim");
+};
+
+// S = Q K^T for one 128-row Q tile and one 128-key K tile, both staged by TMA
+// as K-major rows in 128-byte (or 64-byte) swizzled chunks of CHUNK_BYTES
+// columns; each instruction consumes 32 bytes of the head dimension.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+  using C = Cfg<D, FP8>;
+#pragma unroll
+  for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
+    const uint32_t byte_k = ks * 32;
+    const uint32_t chunk = byte_k / C::CHUNK_BYTES;
+    const uint32_t within = byte_k % C::CHUNK_BYTES;
+    const uint64_t a = make_sdesc(q_smem + chunk * C::Q_CHUNK_BYTES + within, 16,
+                                  8 * C::CHUNK_BYTES, C::SWZ_CODE);
+    const uint64_t b = make_sdesc(k_smem + chunk * C::KV_CHUNK_BYTES + within, 16,
+                                  8 * C::CHUNK_BYTES, C::SWZ_CODE);
+    if constexpr (FP8) mma_f8_ss(d_tmem, a, b, C::IDESC_S, ks > 0);
+    else mma_f16_ss(d_tmem, a, b, C::IDESC_S, ks > 0);
+  }
+}
+
+// O (+)= P V: P (128 x 128 keys) in tensor memory, packed along the keys;
+// V tile staged by TMA with d contiguous (MN-major B operand): the leading
+// byte offset steps between d-chunks, the stride byte offset between groups
+// of 8 keys; each instruction consumes MMA_K keys.
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  using C = Cfg<D, FP8>;
+#pragma unroll
+  for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
+    const uint64_t b = make_sdesc(v_smem + ks * C::MMA_K * C::CHUNK_BYTES, C::KV_CHUNK_BYTES,
+                                  8 * C::CHUNK_BYTES, C::SWZ_CODE);
+    const uint32_t a = p_tmem + ks * C::P_COLS_PER_KSTEP;
+    const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
+    if constexpr (FP8) mma_f8_ts(d_tmem, a, b, C::IDESC_PV, acc);
+    else mma_f16_ts(d_tmem, a, b, C::IDESC_PV, acc);
+  }
+}
+
+struct Unit {
+  int b, hq, hkv, row0;
+  int n[2];  // K/V tiles needed by Q tile 0 / 1 (0 = tile idle or fully masked)
+  int nmax;
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Work unit u -> coordinates. Units are ordered with the largest query rows
+// first (the most K/V tiles under a causal mask); consecutive units differ in
+// hq first, so query heads sharing a KV head run on neighbouring CTAs.
+__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& P) {
+  Unit U;
+  const int bh_total = P.B * P.Hq;
+  const int level = u / bh_total;
+  const int bh = u - level * bh_total;
+  U.b = bh / P.Hq;
+  U.hq = bh - U.b * P.Hq;
+  U.hkv = U.hq / P.group;
+  U.row0 = (P.n_qp - 1 - level) * UNIT_ROWS;
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int r0 = U.row0 + t * BM;
+    int n = 0;
+    if (r0 < P.Sq) {
+      if (!P.causal) {
+        n = P.nkv;
+      } else {
+        const int rl = min(r0 + BM, P.Sq) - 1;
+        const int lim = rl + (P.Sk - P.Sq) + 1;  // keys visible to the last row
+        n = lim <= 0 ? 0 : min(ceil_div(lim, BN), P.nkv);
+      }
+    }
+    U.n[t] = n;
+  }
+  U.nmax = max(U.n[0], U.n[1]);
+  return U;
+}
+
+struct Ctl {
+  uint32_t tmem_base;
+  uint32_t abort_flag;
+};
+
+// Bounded wait on an mbarrier phase. Returns false when the CTA is aborting
+// (another role gave up) or when this wait ran past the limit (it then starts
+// the abort and records the timeout).
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile Ctl* ctl,
+                                             const FwdParams& P) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (ctl->abort_flag) return false;
+    if (global_timer_ns() - t0 > P.timeout_ns) {
+      ctl->abort_flag = 1u;
+      atomicCAS(P.status, 0, STATUS_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Bounded wait used while draining: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const FwdParams& P) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > P.timeout_ns) {
+      atomicCAS(P.status, 0, STATUS_TIMEOUT);
+      return;
+    }
+  }
+}
+
+template <int D, bool FP8>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
+                    const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
+  using C = Cfg<D, FP8>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + C::OFF_BAR;
+  const uint32_t BAR_Q_FULL = bar0;
+  const uint32_t BAR_Q_EMPTY = bar0 + 8;
+  const uint32_t BAR_KV_FULL = bar0 + 16;                     // + 8 * slot
+  const uint32_t BAR_KV_EMPTY = BAR_KV_FULL + 8 * C::NSLOT;   // + 8 * slot
+  const uint32_t BAR_S_FULL = BAR_KV_EMPTY + 8 * C::NSLOT;    // + 8 * t
+  const uint32_t BAR_P_FULL = BAR_S_FULL + 16;                // + 8 * t
+  const uint32_t BAR_O_FULL = BAR_P_FULL + 16;                // + 8 * t
+  const uint32_t BAR_DRAIN = BAR_O_FULL + 16;
+  volatile Ctl* ctl = reinterpret_cast<volatile Ctl*>(smem + C::OFF_MISC);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // ---------------------------------------------------------------- setup
+  if (warp == WARP_LOAD && lane == 0) {
+    mbar_init(BAR_Q_FULL, 1);
+    mbar_init(BAR_Q_EMPTY, 1);
+    for (int s = 0; s < C::NSLOT; ++s) {
+      mbar_init(BAR_KV_FULL + 8 * s, 1);
+      mbar_init(BAR_KV_EMPTY + 8 * s, 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(BAR_S_FULL + 8 * t, 1);
+      mbar_init(BAR_P_FULL + 8 * t, BM);
+      mbar_init(BAR_O_FULL + 8 * t, 1);
+    }
+    mbar_init(BAR_DRAIN, 1);
+    ctl->abort_flag = 0u;
+    fence_barrier_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  if (warp == WARP_MMA) {
+    tmem_alloc(sbase + C::OFF_MISC, C::TMEM_COLS);  // writes ctl->tmem_base
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == WARP_LOAD) {
+    // ------------------------------------------------------- TMA producer
+    if (lane == 0) {
+      uint32_t it = 0, qit = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
+        const Unit U = decode_unit(u, P);
+        if (U.nmax == 0) continue;
+        if (!wait_bounded(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
+        const int nq = (U.n[0] > 0) + (U.n[1] > 0);
+        mbar_arrive_expect_tx(BAR_Q_FULL, nq * C::Q_TILE_BYTES);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (U.n[t] == 0) continue;
+#pragma unroll
+          for (int c = 0; c < C::NCHUNK; ++c)
+            tma_load_4d(sbase + C::OFF_Q + t * C::Q_TILE_BYTES + c * C::Q_CHUNK_BYTES, &tm_q,
+                        BAR_Q_FULL, c * C::CHUNK_ELEMS, U.hq, U.row0 + t * BM, U.b);
+        }
+        ++qit;
+        for (int j = 0; ok && j < U.nmax; ++j) {
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {
+            const uint32_t slot = it % C::NSLOT;
+            if (!wait_bounded(BAR_KV_EMPTY + 8 * slot, ((it / C::NSLOT) & 1u) ^ 1u, ctl, P)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(BAR_KV_FULL + 8 * slot, C::KV_TILE_BYTES);
+#pragma unroll
+            for (int c = 0; c < C::NCHUNK; ++c)
+              tma_load_4d(sbase + C::OFF_KV + slot * C::KV_TILE_BYTES + c * C::KV_CHUNK_BYTES,
+                          kv ? &tm_v : &tm_k, BAR_KV_FULL + 8 * slot, c * C::CHUNK_ELEMS, U.hkv,
+                          j * BN, U.b);
+            ++it;
+          }
+        }
+      }
+      // Drain: every copy issued must land before the CTA may exit.
+      for (uint32_t s = 0; s < C::NSLOT; ++s) {
+        if (it > s) {
+          const uint32_t fills = (it - 1 - s) / C::NSLOT + 1;
+          drain_wait(BAR_KV_FULL + 8 * s, (fills - 1) & 1u, P);
+        }
+      }
+      if (qit > 0) drain_wait(BAR_Q_FULL, (qit - 1) & 1u, P);
+    }
+    __syncwarp();
+  } else if (warp == WARP_MMA) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t it = 0, qit = 0;
+      uint32_t pc[2] = {0u, 0u};
+      bool ok = true;
+      const uint32_t q_smem = sbase + C::OFF_Q;
+      const uint32_t kv_smem = sbase + C::OFF_KV;
+
+      auto issue_s = [&](int t, uint32_t slot) {
+        issue_qk<D, FP8>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
+                         kv_smem + slot * C::KV_TILE_BYTES);
+      };
+      auto issue_o = [&](int t, uint32_t slot, bool acc) {
+        issue_pv<D, FP8>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
+                         kv_smem + slot * C::KV_TILE_BYTES, acc);
+      };
+
+      for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
+        const Unit U = decode_unit(u, P);
+        if (U.nmax == 0) continue;
+        if (!wait_bounded(BAR_Q_FULL, qit & 1u, ctl, P)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const uint32_t slot = it % C::NSLOT;
+          if (!wait_bounded(BAR_KV_FULL + 8 * slot, (it / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+            if (U.n[t] > 0) {
+              issue_s(t, slot);
+              tc_commit(BAR_S_FULL + 8 * t);
+            }
+          tc_commit(BAR_KV_EMPTY + 8 * slot);
+          if (U.nmax == 1) tc_commit(BAR_Q_EMPTY);
+        }
+        for (int j = 0; j < U.nmax; ++j) {
+          const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
+          const uint32_t itk = itv + 1, kslot = itk % C::NSLOT;
+          const bool more = j + 1 < U.nmax;
+          if (!wait_bounded(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            if (j < U.n[t]) {
+              if (!wait_bounded(BAR_P_FULL + 8 * t, pc[t] & 1u, ctl, P)) { ok = false; break; }
+              ++pc[t];
+              tc_fence_after();
+              issue_o(t, vslot, j > 0);
+              if (j == U.n[t] - 1) tc_commit(BAR_O_FULL + 8 * t);
+            }
+            if (t == 0 && more) {
+              if (!wait_bounded(BAR_KV_FULL + 8 * kslot, (itk / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+              tc_fence_after();
+            }
+            if (j + 1 < U.n[t]) {
+              issue_s(t, kslot);
+              tc_commit(BAR_S_FULL + 8 * t);
+            }
+          }
+          if (!ok) break;
+          tc_commit(BAR_KV_EMPTY + 8 * vslot);
+          if (more) {
+            tc_commit(BAR_KV_EMPTY + 8 * kslot);
+            if (j + 2 == U.nmax) tc_commit(BAR_Q_EMPTY);
+          }
+        }
+        it += 2 * U.nmax;
+        ++qit;
+      }
+      // Drain: all issued MMAs complete before the tensor memory is freed.
+      tc_commit(BAR_DRAIN);
+      drain_wait(BAR_DRAIN, 0u, P);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int t = warp >> 2;           // Q tile handled by this warpgroup
+    const int quad = warp & 3;         // TMEM lane quadrant of this warp
+    const int rloc = quad * 32 + lane; // row within the tile == TMEM lane
+    const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t col_s = C::COL_S0 + t * BN;
+    const uint32_t col_o = C::COL_O0 + t * D;
+    const float cs = P.scale_log2;
+    const int nblk_q = ceil_div(P.Sq, FP8_BLOCK);
+    const int nblk_k = ceil_div(P.Sk, FP8_BLOCK);
+    uint32_t sc = 0, oc = 0;  // phase counters of s_full[t], o_full[t]
+    bool ok = true;
+
+    for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
+      const Unit U = decode_unit(u, P);
+      const int tile_row0 = U.row0 + t * BM;
+      if (tile_row0 >= P.Sq) continue;  // idle tile
+      const int row = tile_row0 + rloc;
+      const bool row_ok = row < P.Sq;
+      const int n = t ? U.n[1] : U.n[0];
+      float m_run = -INFINITY, l_run = 0.f;
+      float cq = cs;         // per-row exponent scale (FP8: times the Q block scale)
+      float v_ref = 1.f;     // FP8: largest V block scale of this KV head
+      const float* ks_row = nullptr;
+      const float* vs_row = nullptr;
+      if constexpr (FP8) {
+        if (P.q_scale != nullptr) {  // null scales mean all block scales are 1
+          const float sq = row_ok ? P.q_scale[(static_cast<size_t>(U.b) * P.Hq + U.hq) * nblk_q +
+                                              row / FP8_BLOCK]
+                                  : 1.f;
+          cq = cs * sq;
+          ks_row = P.k_scale + (static_cast<size_t>(U.b) * P.Hkv + U.hkv) * nblk_k;
+          vs_row = P.v_scale + (static_cast<size_t>(U.b) * P.Hkv + U.hkv) * nblk_k;
+          float vm = 0.f;
+          for (int i = 0; i < nblk_k; ++i) vm = fmaxf(vm, vs_row[i]);
+          v_ref = vm > 0.f ? vm : 1.f;
+        }
+      }
+
+      for (int j = 0; j < n; ++j) {
+        bool w = wait_bounded(BAR_S_FULL + 8 * t, sc & 1u, ctl, P);
+        ++sc;
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+
+        float s[BN];
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i) {
+          uint32_t r[32];
+          tmem_ld32(t_lane + col_s + 32 * i, r);
+#pragma unroll
+          for (int c = 0; c < 32; ++c) s[32 * i + c] = __uint_as_float(r[c]);
+        }
+        // mask: keys past Sk, and (causal) keys after row + Sk - Sq
+        int vis = P.Sk - j * BN;
+        if (P.causal) vis = min(vis, row + (P.Sk - P.Sq) - j * BN + 1);
+        if (vis < BN) {
+#pragma unroll
+          for (int c = 0; c < BN; ++c)
+            if (c >= vis) s[c] = -INFINITY;
+        }
+        // per-column-half exponent scales
+        float c_lo = cq, c_hi = cq, r_lo = 1.f, r_hi = 1.f;
+        if (FP8 && ks_row != nullptr) {
+          const int kb0 = 2 * j, kb1 = 2 * j + 1;
+          c_lo = cq * ks_row[kb0];
+          c_hi = cq * (kb1 < nblk_k ? ks_row[kb1] : 1.f);
+          r_lo = vs_row[kb0] / v_ref;
+          r_hi = (kb1 < nblk_k ? vs_row[kb1] : v_ref) / v_ref;
+        }
+        // tile row max (in log2 units)
+        float mx_lo = s[0], mx_hi = s[BN / 2];
+        {
+          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+#pragma unroll
+          for (int c = 4; c < BN / 2; c += 4) {
+            a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
+            a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
+          }
+          mx_lo = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
+          float b0 = s[BN / 2], b1 = s[BN / 2 + 1], b2 = s[BN / 2 + 2], b3 = s[BN / 2 + 3];
+#pragma unroll
+          for (int c = BN / 2 + 4; c < BN; c += 4) {
+            b0 = fmaxf(b0, s[c]); b1 = fmaxf(b1, s[c + 1]);
+            b2 = fmaxf(b2, s[c + 2]); b3 = fmaxf(b3, s[c + 3]);
+          }
+          mx_hi = fmaxf(fmaxf(b0, b1), fmaxf(b2, b3));
+        }
+        const float m_tile = fmaxf(mx_lo * c_lo, mx_hi * c_hi);
+        const float m_new = fmaxf(m_run, m_tile);
+        const bool need = (m_new - m_run) > RESCALE_LOG2;  // false when both are -inf
+        float factor = 1.f;
+        if (need) {
+          factor = ex2_approx(m_run - m_new);
+          l_run *= factor;
+          m_run = m_new;
+        }
+        const float msafe = (m_run == -INFINITY) ? 0.f : m_run;
+        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
+        if constexpr (!FP8) {
+          // 64 keys -> 32 packed columns per store, so the P registers of one
+          // half are free before the next half is computed
+#pragma unroll
+          for (int i = 0; i < BN / 64; ++i) {
+            const float cc = (i < BN / 128) ? c_lo : c_hi;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 32; c += 2) {
+              const int e = 64 * i + 2 * c;
+              const float p0 = ex2_approx(fmaf(s[e], cc, -msafe));
+              const float p1 = ex2_approx(fmaf(s[e + 1], cc, -msafe));
+              const float p2 = ex2_approx(fmaf(s[e + 2], cc, -msafe));
+              const float p3 = ex2_approx(fmaf(s[e + 3], cc, -msafe));
+              l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+              pk[c] = pack_bf16x2(p0, p1);
+              pk[c + 1] = pack_bf16x2(p2, p3);
+            }
+            tmem_st32(t_lane + col_s + 32 * i, pk);
+          }
+        } else {
+          uint32_t pk[BN / 4];
+#pragma unroll
+          for (int c = 0; c < BN / 4; ++c) {
+            const bool lo = 4 * c < BN / 2;
+            const float cc = lo ? c_lo : c_hi;
+            const float rr = lo ? r_lo : r_hi;
+            const float p0 = ex2_approx(fmaf(s[4 * c], cc, -msafe));
+            const float p1 = ex2_approx(fmaf(s[4 * c + 1], cc, -msafe));
+            const float p2 = ex2_approx(fmaf(s[4 * c + 2], cc, -msafe));
+            const float p3 = ex2_approx(fmaf(s[4 * c + 3], cc, -msafe));
+            l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+            pk[c] = pack_e4m3x4(p0 * rr, p1 * rr, p2 * rr, p3 * rr);
+          }
+          tmem_st32(t_lane + col_s, pk);
+        }
+        l_run += (l0 + l1) + (l2 + l3);
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O_t holds the sum over earlier tiles: S_t(j) completing implies
+          // the previous O_t += P V has completed as well. Done after P is
+          // written so the score registers are already free.
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint32_t r[32];
+            tmem_ld32(t_lane + col_o + 32 * i, r);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
+            tmem_st32(t_lane + col_o + 32 * i, r);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR_P_FULL + 8 * t);
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------- epilogue
+      const size_t lse_idx = (static_cast<size_t>(U.b) * P.Hq + U.hq) * P.Sq + row;
+      __nv_bfloat16* orow =
+          P.o + ((static_cast<size_t>(U.b) * P.Sq + row) * P.Hq + U.hq) * static_cast<size_t>(D);
+      if (n > 0) {
+        bool w = wait_bounded(BAR_O_FULL + 8 * t, oc & 1u, ctl, P);
+        ++oc;
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        const float inv = l_run > 0.f ? v_ref / l_run : 0.f;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          uint32_t r[32];
+          tmem_ld32(t_lane + col_o + 32 * i, r);
+          uint32_t pk[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c)
+            pk[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv);
+          if (row_ok) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+          }
+        }
+        if (row_ok) P.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+      } else if (row_ok) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+        P.lse[lse_idx] = -INFINITY;
+      }
+    }
+  }
+
+  // --------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == WARP_MMA) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+}  // namespace attnb3

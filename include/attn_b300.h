@@ -1,0 +1,133 @@
+/*
+ * attn_b300.h -- C ABI of the B300 (sm_103a) exact attention forward library
+ * (libattn_b300.so).
+ *
+ * The operation (FlashAttention-3 deep dive, techknowgenie.com/posts/
+ * 109164421204410442, introduction and section "3-stage asynchronous software
+ * pipelining"): exact softmax attention, computed tile by tile with an online
+ * softmax so the Sq x Sk score matrix never reaches device memory:
+ *
+ *     O[b,i,hq,:] = sum_j softmax_j( scale * Q[b,i,hq,:] . K[b,j,hkv,:] ) V[b,j,hkv,:]
+ *     LSE[b,hq,i] = ln sum_j exp( scale * Q[b,i,hq,:] . K[b,j,hkv,:] )
+ *
+ * with j restricted to the visible keys. The pages do not define the causal
+ * alignment, grouped-query heads or the LSE output; this library reads them as:
+ *   - causal: key j is visible to query i iff j <= i + Sk - Sq (bottom-right);
+ *   - GQA: hkv = hq / (Hq / Hkv), i.e. consecutive query heads share a KV head;
+ *   - LSE is the natural logarithm; a row with no visible key gets O = 0 and
+ *     LSE = -inf.
+ *
+ * Layouts (all dense, row-major, no padding):
+ *   q, o : [B, Sq, Hq, d]     k, v : [B, Sk, Hkv, d]     lse : [B, Hq, Sq] fp32
+ * O is always written as bf16.
+ *
+ * Ownership and execution: every pointer is a DEVICE pointer owned by the
+ * caller. The library allocates no device memory, holds no per-call workspace
+ * and keeps no state between calls except a cached driver entry point, the
+ * per-device kernel attributes and one device status word (below). Work is
+ * enqueued on `stream` (0 = legacy default stream) and the call returns
+ * without synchronising; device-side failures surface through
+ * attn_device_status(). All entry points are thread-safe.
+ *
+ * Error behaviour: argument checks run on the host before anything is
+ * enqueued; a failed check returns its code and launches nothing.
+ */
+#ifndef ATTN_B300_H
+#define ATTN_B300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* attn_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0,
+                                 scale not finite and > 0, an index that does
+                                 not fit in 32 bits */
+    ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, unknown dtype, device is
+                                 not compute capability 10.3 (B300) */
+    ATTN_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned (TMA rule) */
+    ATTN_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
+    ATTN_ERR_TIMEOUT = 5      /* a kernel-internal wait gave up (watchdog);
+                                 reported by attn_device_status() only */
+} attn_status_t;
+
+typedef enum {
+    ATTN_BF16 = 0,    /* q, k, v are bf16 */
+    ATTN_FP8_E4M3 = 1 /* q, k, v are OCP E4M3 codes with unit scales */
+} attn_dtype_t;
+
+/* Rows of one FP8 scale block (per batch, head and block of consecutive
+ * sequence rows; all d columns share the scale). */
+#define ATTN_FP8_BLOCK_ROWS 64
+
+/*
+ * attn_fwd -- fused attention forward.
+ *   q, k, v : device inputs in the layouts above, element type `dtype`
+ *   o       : device output, bf16 [B, Sq, Hq, d]
+ *   lse     : device output, fp32 [B, Hq, Sq]
+ *   B, Hq, Hkv, Sq, Sk, d : sizes; Hq % Hkv == 0; d in {64, 128}
+ *   causal  : 0 or non-zero (bottom-right causal mask)
+ *   scale   : softmax scale applied to Q.K (finite, > 0; usually 1/sqrt(d))
+ *   dtype   : attn_dtype_t; ATTN_FP8_E4M3 behaves as attn_fwd_fp8 with all
+ *             block scales equal to 1
+ * Every element count (B*S*H*d per tensor) must be below 2^31.
+ * Returns an attn_status_t.
+ */
+int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
+             int B, int Hq, int Hkv, int Sq, int Sk, int d,
+             int causal, float scale, int dtype, attn_stream_t stream);
+
+/*
+ * attn_fwd_fp8 -- attention forward on E4M3 inputs with per-block scales
+ * (FlashAttention-3 deep dive, section "FP8 low-precision arithmetic and
+ * numerical stability": block quantisation with one scale per tile block,
+ * FP8 products with fp32 accumulation, base-2 exponentials).
+ *   q, k, v    : E4M3 codes, layouts as above
+ *   q_scale    : fp32 [B, Hq,  ceil(Sq / 64)]
+ *   k_scale,
+ *   v_scale    : fp32 [B, Hkv, ceil(Sk / 64)]
+ * The value of an element is code * scale of its (b, h, row / 64) block.
+ * Scales must be finite and > 0. Other arguments as attn_fwd.
+ */
+int attn_fwd_fp8(const void* q, const void* k, const void* v,
+                 const float* q_scale, const float* k_scale, const float* v_scale,
+                 void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
+                 int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_quantize_fp8_e4m3 -- block quantiser producing attn_fwd_fp8 inputs
+ * (same section of the FlashAttention-3 deep dive: per-block scale from the
+ * block's local maximum).
+ *   x     : device fp32 [B, S, H, d]
+ *   codes : device uint8 [B, S, H, d] (E4M3)
+ *   scale : device fp32 [B, H, ceil(S / 64)]
+ * Per block of 64 rows of one head: s = amax / 448 (fp32 division), or 1 when
+ * amax == 0; code = round-to-nearest-even, saturating E4M3 of x / s (fp32
+ * IEEE division). A ragged last block uses its own rows only.
+ * Sizes as attn_fwd (d in {64, 128}). Returns an attn_status_t.
+ */
+int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale,
+                           int B, int S, int H, int d, attn_stream_t stream);
+
+/*
+ * attn_device_status -- synchronises `stream`, then returns and clears the
+ * device status word: ATTN_OK, ATTN_ERR_TIMEOUT if a kernel's bounded wait
+ * gave up since the last call (the kernel then abandoned its work and its
+ * outputs are undefined), or ATTN_ERR_CUDA if the synchronisation failed.
+ * The word is shared by every launch on the current device.
+ */
+int attn_device_status(attn_stream_t stream);
+
+/* attn_status_string -- static, human-readable name of a status code. */
+const char* attn_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_B300_H */

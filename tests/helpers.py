@@ -1,0 +1,45 @@
+"""Shared test helpers: tolerances and GPU plumbing (no attention arithmetic)."""
+import numpy as np
+import pytest
+
+
+def require_gpu():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("this test needs a CUDA device")
+    return torch
+
+
+def bf16_atol(ref):
+    """Per-element bound for bf16 O: max(1e-2, one bf16 ulp of the reference).
+    The output rounding alone is half an ulp, which exceeds 1e-2 once |O| >= 4."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ref, 1e-30)))
+    return np.maximum(1e-2, np.exp2(e - 7))
+
+
+def assert_o_close(o_gpu, o_ref, kind="bf16"):
+    o_gpu = np.asarray(o_gpu, dtype=np.float64)
+    o_ref = np.asarray(o_ref, dtype=np.float64)
+    assert np.isfinite(o_gpu).all(), "non-finite output"
+    err = np.abs(o_gpu - o_ref)
+    if kind == "bf16":
+        tol = bf16_atol(o_ref)
+    else:
+        tol = np.full_like(o_ref, 6e-2)
+    bad = err > tol
+    assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside tolerance; "
+                           f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")
+    return float(err.max())
+
+
+def assert_lse_close(l_gpu, l_ref, tol=1e-3):
+    l_gpu = np.asarray(l_gpu, dtype=np.float64)
+    l_ref = np.asarray(l_ref, dtype=np.float64)
+    inf_ref = np.isneginf(l_ref)
+    assert (np.isneginf(l_gpu) == inf_ref).all(), "-inf rows differ"
+    if (~inf_ref).any():
+        err = np.abs(l_gpu[~inf_ref] - l_ref[~inf_ref])
+        assert err.max() <= tol, f"LSE max err {err.max():.3e}"
+        return float(err.max())
+    return 0.0

@@ -1,0 +1,56 @@
+"""Single-tile checks of the two tcgen05 contraction forms the kernel uses
+(S = Q K^T with both operands K-major in shared memory; O = P V with P in
+tensor memory and V d-contiguous), against torch matmul in fp32."""
+import ctypes
+import os
+
+import pytest
+
+from tests.helpers import require_gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+LIB = os.path.join(ROOT, "exact_attention_forward_14_b300", "libattn_selftest.so")
+
+
+def _single_tile(form, fp8):
+    torch = require_gpu()
+    lib = ctypes.CDLL(LIB)
+    lib.attn_selftest_umma.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 5
+    lib.attn_selftest_umma.restype = ctypes.c_int
+    g = torch.Generator().manual_seed(100 + 2 * form + fp8)
+    a32 = torch.randn(128, 128, generator=g)
+    b32 = torch.randn(128, 128, generator=g)
+    if form == 1:
+        a32 = a32.abs()  # P is non-negative
+    if fp8:
+        a = a32.to(torch.float8_e4m3fn)
+        b = b32.to(torch.float8_e4m3fn)
+    else:
+        a = a32.to(torch.bfloat16)
+        b = b32.to(torch.bfloat16)
+    af, bf = a.float(), b.float()
+    ref = af @ bf.T if form == 0 else af @ bf
+    da = a.view(torch.uint8).cuda() if fp8 else a.cuda()
+    db = b.view(torch.uint8).cuda() if fp8 else b.cuda()
+    out = torch.full((128, 128), float("nan"), device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.attn_selftest_umma(form, fp8, da.data_ptr(), db.data_ptr(), out.data_ptr(),
+                                err.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0
+    assert int(err.item()) == 0, "a wait timed out"
+    got = out.cpu()
+    diff = (got - ref).abs().max().item()
+    assert diff < 1e-3 * max(1.0, ref.abs().max().item()), f"max diff {diff}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("form", [0, 1], ids=["qk", "pv"])
+def test_umma_bf16(form):
+    _single_tile(form, 0)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("form", [0, 1], ids=["qk", "pv"])
+def test_umma_fp8(form):
+    _single_tile(form, 1)

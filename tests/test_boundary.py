@@ -1,0 +1,119 @@
+"""C-ABI boundary checks that need no GPU: the library loads, exports every
+entry point the header declares, and rejects bad arguments on the host with
+the documented status codes before touching CUDA."""
+import os
+import re
+
+import pytest
+
+import exact_attention_forward_14_b300 as ea
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "attn_b300.h")
+PKG = os.path.join(ROOT, "exact_attention_forward_14_b300")
+
+# fake, never dereferenced device addresses (16-byte aligned)
+Q, K, V, O, L = 0x10000, 0x20000, 0x30000, 0x40000, 0x50000
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from exact_attention_forward_14_b300 import build
+    build.build()
+    return ea.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return re.findall(r"^\s*(?:int|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_boundary():
+    assert set(declared_functions()) >= {"attn_fwd", "attn_fwd_fp8", "attn_quantize_fp8_e4m3",
+                                         "attn_device_status", "attn_status_string"}
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    names = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
+             3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
+    for code, name in names.items():
+        assert ea.attn_status_string(code) == name
+    assert ea.attn_status_string(99) == "ATTN_ERR_UNKNOWN"
+
+
+def fwd(**kw):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, B=1, Hq=2, Hkv=2, Sq=128, Sk=128, d=128, causal=0,
+             scale=0.1, dtype=ea.ATTN_BF16, stream=0)
+    a.update(kw)
+    return ea.attn_fwd(**a)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(Sk=-1), ea.ATTN_ERR_INVALID_ARG),
+    (dict(Hq=3, Hkv=2), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=-0.5), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("nan")), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=float("inf")), ea.ATTN_ERR_INVALID_ARG),
+    (dict(B=1, Sq=1 << 20, Hq=32, Hkv=32, d=128), ea.ATTN_ERR_INVALID_ARG),  # 2^32 elements
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=7), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(q=Q + 8), ea.ATTN_ERR_MISALIGNED),
+    (dict(v=V + 2), ea.ATTN_ERR_MISALIGNED),
+    (dict(o=O + 4), ea.ATTN_ERR_MISALIGNED),
+    (dict(lse=L + 2), ea.ATTN_ERR_MISALIGNED),
+])
+def test_attn_fwd_rejects_bad_arguments(lib, kw, code):
+    assert fwd(**kw) == code
+
+
+def test_attn_fwd_fp8_requires_scales(lib):
+    args = [Q, K, V, 0x60000, 0x70000, 0x80000, O, L, 1, 2, 2, 128, 128, 128, 0, 0.1]
+    bad = list(args)
+    bad[4] = 0
+    assert ea.attn_fwd_fp8(*bad, stream=0) == ea.ATTN_ERR_INVALID_ARG
+    bad = list(args)
+    bad[3] = 0x60002
+    assert ea.attn_fwd_fp8(*bad, stream=0) == ea.ATTN_ERR_MISALIGNED
+    bad = list(args)
+    bad[13] = 80
+    assert ea.attn_fwd_fp8(*bad, stream=0) == ea.ATTN_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("args,code", [
+    ((0, Q, L, 1, 64, 2, 128), ea.ATTN_ERR_INVALID_ARG),
+    ((Q, Q, L, 1, 0, 2, 128), ea.ATTN_ERR_INVALID_ARG),
+    ((Q, Q, L, 1, 64, 2, 32), ea.ATTN_ERR_UNSUPPORTED),
+    ((Q + 4, K, L, 1, 64, 2, 128), ea.ATTN_ERR_MISALIGNED),
+])
+def test_quantiser_rejects_bad_arguments(lib, args, code):
+    assert ea.attn_quantize_fp8_e4m3(*args, stream=0) == code
+
+
+def test_valid_call_without_a_gpu_fails_loudly(lib):
+    """With no CUDA device the library returns an error: there is no CPU path."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd() in (ea.ATTN_ERR_CUDA, ea.ATTN_ERR_UNSUPPORTED)
+    with pytest.raises(ea.AttnError):
+        ea._check(fwd(), "attn_fwd")
+
+
+def test_product_package_never_touches_the_oracle():
+    for dirpath, _, files in os.walk(PKG):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
+                assert "attn_oracle" not in text and "liboracle" not in text, f
