@@ -1,0 +1,387 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused attention forward on one or more B300s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference]
+
+A step is one attention forward (one ``attn_fwd`` call through the C ABI)
+over the whole workload, inputs resident in device memory. The default
+workload is the long-context prefill shape B=2, H=32, S=8192, d=128, bf16,
+causal. Prints ONE JSON line on rank 0.
+
+With N > 1 (one process per GPU, launched by torch.distributed.run) every rank
+runs the same workload on its own GPU (independent replicas: the heads of
+the batch are independent, nothing is exchanged), timing is bracketed by
+barriers, the time is the max over ranks and ``value`` counts all ranks' work.
+
+``--impl reference`` times the CPU oracle (fp64, the host's cores) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("attention fwd TFLOP/s (4·B·H·Sq·Sk·d, causal halved) "
+          "and % of B300 tensor peak")
+DEFAULT_WORKLOAD = "b2h32s8192d128_causal"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
+                  "exact_attention_forward_14_b300/csrc/ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from a committed ncu capture, only while the
+    kernel sources still match the capture."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        t = json.load(f)
+    entry = t.get(workload)
+    if not entry or entry.get("kernel_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """Samples SM clock and throttle reasons through NVML in a thread."""
+
+    REASONS = {
+        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
+        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
+        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
+        "display_clock_setting": 0x100,
+    }
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.period = period_s
+        self.samples = []
+        self.reasons = set()
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
+        except Exception:  # no NVML: report no clocks
+            self._nvml = None
+
+    def _run(self):
+        nv = self._nvml
+        while not self._stop.is_set():
+            try:
+                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
+                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                for name, bit in self.REASONS.items():
+                    if mask & bit and name != "gpu_idle":
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+        return self
+
+    def __exit__(self, *exc):
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+
+
+# ------------------------------------------------------------ CPU oracle --
+
+def _oracle_inputs(w):
+    """The workload's inputs as raw bits for the oracle (drawn once)."""
+    os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
+    from exact_attention_forward_14_b300 import inputs
+    q, k, v = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
+    return tuple(inputs.bf16_bits(t) for t in (q, k, v))
+
+
+def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = None):
+    """Times the oracle on a row sample of workload w: n_fixed random rows, or
+    a sample grown until it takes ~target_s of CPU work.
+    Returns (flops_of_sample, seconds, n_rows, threads)."""
+    import numpy as np
+    import oracle
+    qb, kb, vb = bits
+
+    def rows_flops(rows):
+        i = rows % w.Sq
+        if w.causal:
+            vis = np.clip(i + (w.Sk - w.Sq) + 1, 0, w.Sk)
+        else:
+            vis = np.full(rows.shape, w.Sk)
+        return float(4.0 * w.d * vis.sum())
+
+    rng = np.random.default_rng(seed)
+    total = w.B * w.Hq * w.Sq
+    n = n_fixed or 64
+    while True:
+        rows = np.sort(rng.choice(total, size=min(n, total), replace=False)).astype(np.int64)
+        t0 = time.perf_counter()
+        oracle.attn_fwd(qb, kb, vb, w.causal, w.scale, rows=rows)
+        dt = time.perf_counter() - t0
+        if n_fixed or dt >= target_s or n >= total:
+            return rows_flops(rows), dt, rows.size, int(os.environ["OMP_NUM_THREADS"])
+        n = int(min(total, max(2 * n, n * target_s / max(dt, 1e-3) * 1.05)))
+
+
+def cpu_baseline(w, target_s: float = 12.0):
+    flops, dt, n, threads = _oracle_sample(w, _oracle_inputs(w), target_s, seed=1)
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} random query rows of all (b, h) of the workload "
+                      f"({flops / 1e9:.1f} GFLOP by the metric's count) in {dt:.1f} s, "
+                      "fp64 two-pass oracle, OpenMP"}
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    per_step = max(0.5, 150.0 / (args.steps + args.warmup))
+    bits = _oracle_inputs(w)
+    _, _, n_step, _ = _oracle_sample(w, bits, per_step, seed=99)  # calibrate the step size
+    flops_t = []
+    for s in range(args.warmup + args.steps):
+        flops, dt, n, threads = _oracle_sample(w, bits, per_step, seed=100 + s, n_fixed=n_step)
+        if s >= args.warmup:
+            flops_t.append((flops, dt, n))
+    tot_f = sum(f for f, _, _ in flops_t)
+    tot_t = sum(t for _, t, _ in flops_t)
+    value = tot_f / tot_t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * tot_t / len(flops_t), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"each step: ~{flops_t[0][2]} random query rows of the "
+                                   "workload through the fp64 oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+            "d": w.d, "causal": w.causal, "dtype": w.dtype,
+            "l2": "inputs larger than L2 (no flush)"}
+
+
+# ------------------------------------------------------------- GPU path --
+
+def run_ours(args, w):
+    import torch
+    import exact_attention_forward_14_b300 as ea
+    from exact_attention_forward_14_b300 import inputs
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+
+    # inputs: seeded CPU draw, then resident on the device
+    if w.dtype == "e4m3":
+        qf, kf, vf = inputs.draw_workload_f32(w)
+        host = None
+        q8, qs = ea.quantize_fp8(qf.to(dev))
+        k8, ks = ea.quantize_fp8(kf.to(dev))
+        v8, vs = ea.quantize_fp8(vf.to(dev))
+        dev_in = (q8, k8, v8, qs, ks, vs)
+        del qf, kf, vf
+    else:
+        hq, hk, hv = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
+        host = tuple(t.pin_memory() for t in (hq, hk, hv))
+        dev_in = tuple(t.to(dev) for t in host)
+    o = torch.empty((w.B, w.Sq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        if w.dtype == "e4m3":
+            q8, k8, v8, qs, ks, vs = dev_in
+            rc = ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk,
+                                 w.d, w.causal, w.scale, stream)
+        else:
+            q, k, v = dev_in
+            rc = ea.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal,
+                             w.scale, ea.ATTN_BF16, stream)
+        if rc != ea.ATTN_OK:
+            raise ea.AttnError(rc, "attn_fwd")
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    st = ea.attn_device_status(stream)
+    if st != ea.ATTN_OK:
+        raise ea.AttnError(st, "warm-up")
+
+    # timed region: K back-to-back launches, an event pair around each
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clocks:
+        t0.record(stream)
+        for a, b in ev:
+            a.record(stream)
+            step()
+            b.record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if dist is not None:
+        dist.barrier()
+    st = ea.attn_device_status(stream)
+    if st != ea.ATTN_OK:
+        raise ea.AttnError(st, "timed region")
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    if dist is not None:
+        tt = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    flops = w.flops()
+    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs -> device -> kernel
+    # -> O and LSE back to pinned host memory, every step
+    e2e = None
+    if host is not None:
+        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+        e_steps = max(3, min(args.steps, 20))
+        dq, dk, dv = dev_in
+        for it in range(e_steps + 2):
+            if it == 2:
+                if dist is not None:
+                    dist.barrier()
+                torch.cuda.synchronize(dev)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            dq.copy_(host[0], non_blocking=True)
+            dk.copy_(host[1], non_blocking=True)
+            dv.copy_(host[2], non_blocking=True)
+            step()
+            ho.copy_(o, non_blocking=True)
+            hl.copy_(lse, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e_ms = e0.elapsed_time(e1)
+        if dist is not None:
+            tt = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        h2d = sum(t.numel() * t.element_size() for t in host)
+        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
+        e2e = {"value": world * flops * e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms / e_steps}
+
+    if rank != 0:
+        if dist is not None:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peaks_src = load_peaks()
+    mean_launch_ms = statistics.mean(launch_ms)
+    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
+    roofline = {
+        "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+        "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+        "kernel": f"attn_fwd_kernel<{w.d},{'true' if w.dtype == 'e4m3' else 'false'}>",
+        "peak_source": (f"{peaks_src} bf16 burst" if w.dtype != "e4m3"
+                        else f"{peaks_src} bf16 burst x 2 (nominal fp8/bf16 ratio)"),
+        "frac_of_sustained": achieved / (peaks.get("bf16_tflops_sustained", peak) *
+                                         (2.0 if w.dtype == "e4m3" else 1.0)),
+        "launch_ms_median": statistics.median(launch_ms),
+    }
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if w.dtype == "e4m3" else "bf16", "data": "synthetic",
+        "config": workload_config(w), "clocks": clocks.summary(), "e2e": e2e,
+        "gpu_launches": args.steps, "roofline": roofline,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w)
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true",
+                    help="skip the CPU oracle timing (e.g. under a profiler)")
+    args = ap.parse_args(argv)
+    from exact_attention_forward_14_b300 import inputs
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -7,7 +7,7 @@ import pytest
 
 import exact_attention_forward_14_b300 as ea
 from exact_attention_forward_14_b300 import inputs
-from tests.helpers import assert_lse_close, assert_o_close, require_gpu
+from tests.helpers import assert_lse_close, assert_o_close, bf16_atol, require_gpu
 
 # (B, Hq, Hkv, Sq, Sk, d, causal): several tiles, ragged tails, GQA, Sq != Sk,
 # fully masked rows (causal with Sq > Sk), single row / single key.
@@ -59,11 +59,18 @@ def test_bf16_large_scores_exercise_rescaling(oracle_mod):
     ramp = torch.linspace(0.0, 3.0, S).view(1, S, 1, 1)
     k = (torch.randn(B, S, H, d, generator=g) * (0.5 + ramp)).to(torch.bfloat16)
     v = torch.randn(B, S, H, d, generator=g).to(torch.bfloat16)
+    vmax = float(v.float().abs().max())
     for causal in (False, True):
         o, lse = run_bf16(torch, q, k, v, causal, 0.125)
         o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
                                              inputs.bf16_bits(v), causal, 0.125)
-        assert_o_close(o, o_ref)
+        # With a few dominant keys the bf16 rounding of P (relative 2^-9 per
+        # weight, the normaliser kept in fp32) moves O by up to 2^-9 * max|V|
+        # on top of the output's own half-ulp rounding; a rescaling mistake
+        # would be off by O(1).
+        err = np.abs(o - o_ref)
+        bound = 2.0 ** -9 * vmax + bf16_atol(o_ref) / 2 + 1e-3
+        assert (err <= bound).all(), f"max err {err.max():.3e}"
         assert_lse_close(lse, lse_ref)
 
 
