@@ -84,28 +84,37 @@ class ClockSampler:
         self.samples = []
         self.reasons = set()
         self.max_mhz = None
+        self.error = None
         self._stop = threading.Event()
         self._thread = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(device_index)
+            # NVML numbers devices physically; honour CUDA_VISIBLE_DEVICES
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+            idx = device_index
+            if vis and vis.split(",")[device_index].strip().isdigit():
+                idx = int(vis.split(",")[device_index])
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(idx)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-        except Exception:  # no NVML: report no clocks
+            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        except Exception as e:  # no NVML: report no clocks, say why
             self._nvml = None
+            self.error = f"{type(e).__name__}: {e}"
 
     def _run(self):
         nv = self._nvml
         while not self._stop.is_set():
             try:
                 self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                mask = nv.nvmlDeviceGetCurrentClocksEventReasons(self._h)
+                mask = self._reasons_fn(self._h)
                 for name, bit in self.REASONS.items():
                     if mask & bit and name != "gpu_idle":
                         self.reasons.add(name)
-            except Exception:
-                pass
+            except Exception as e:
+                self.error = f"{type(e).__name__}: {e}"
             time.sleep(self.period)
 
     def __enter__(self):
@@ -120,11 +129,12 @@ class ClockSampler:
             self._thread.join()
 
     def summary(self):
-        if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "samples": 0}
-        return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
+               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+               "samples": len(self.samples), "source": "nvml"}
+        if self.error:
+            out["error"] = self.error
+        return out
 
 
 # ------------------------------------------------------------ CPU oracle --

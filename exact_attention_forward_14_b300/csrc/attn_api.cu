@@ -115,14 +115,15 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
   P.Sk = Sk;
   P.group = Hq / Hkv;
   P.n_qp = (Sq + attnb3::UNIT_ROWS - 1) / attnb3::UNIT_ROWS;
+  P.npair = (P.n_qp + 1) / 2;
   P.nkv = (Sk + attnb3::BN - 1) / attnb3::BN;
-  P.num_units = B * Hq * P.n_qp;
+  P.num_items = B * Hq * P.npair;
   P.causal = causal ? 1 : 0;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.timeout_ns = kWaitLimitNs;
   P.status = di->status;
 
-  const int grid = P.num_units < di->num_sms ? P.num_units : di->num_sms;
+  const int grid = P.num_items < di->num_sms ? P.num_items : di->num_sms;
   kern<<<grid, attnb3::NUM_THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

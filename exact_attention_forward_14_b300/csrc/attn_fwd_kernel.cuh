@@ -73,9 +73,10 @@ struct FwdParams {
   const float* v_scale;  // FP8 only: [B, Hkv, ceil(Sk/64)]
   int B, Hq, Hkv, Sq, Sk;
   int group;      // Hq / Hkv
-  int n_qp;       // ceil(Sq / UNIT_ROWS)
+  int n_qp;       // ceil(Sq / UNIT_ROWS): units (levels) per (b, hq)
+  int npair;      // ceil(n_qp / 2): work items per (b, hq)
   int nkv;        // ceil(Sk / BN)
-  int num_units;  // B * Hq * n_qp
+  int num_items;  // B * Hq * npair
   int causal;
   float scale_log2;  // softmax scale * log2(e)
   unsigned long long timeout_ns;
@@ -170,18 +171,24 @@ struct Unit {
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
-// Work unit u -> coordinates. Units are ordered with the largest query rows
-// first (the most K/V tiles under a causal mask); consecutive units differ in
-// hq first, so query heads sharing a KV head run on neighbouring CTAs.
-__device__ __forceinline__ Unit decode_unit(int u, const FwdParams& P) {
-  Unit U;
-  const int bh_total = P.B * P.Hq;
-  const int level = u / bh_total;
-  const int bh = u - level * bh_total;
+// Work items and units. A unit is (b, hq, 256 query rows); the units of one
+// (b, hq) are its n_qp "levels" (level L covers rows [256 L, 256 L + 256)).
+// A work item pairs level n_qp-1-p with level p of the same (b, hq), so under
+// a causal mask every item costs the same number of K/V tiles (a heavy unit
+// plus its mirror) and a static round-robin over items balances the CTAs.
+// Items are numbered (b, hq)-major with hq fastest: the CTAs running at the
+// same time cover only a few heads (query heads sharing a KV head are
+// adjacent), so those heads' K/V tiles are re-read from L2, not HBM.
+// Returns false when item w has no k-th unit (odd n_qp, middle level).
+__device__ __forceinline__ bool decode_unit(int w, int k, const FwdParams& P, Unit& U) {
+  const int bh = w / P.npair;
+  const int p = w - bh * P.npair;
+  const int level = k == 0 ? P.n_qp - 1 - p : p;
+  if (k == 1 && level == P.n_qp - 1 - p) return false;
   U.b = bh / P.Hq;
   U.hq = bh - U.b * P.Hq;
   U.hkv = U.hq / P.group;
-  U.row0 = (P.n_qp - 1 - level) * UNIT_ROWS;
+  U.row0 = level * UNIT_ROWS;
 #pragma unroll
   for (int t = 0; t < 2; ++t) {
     const int r0 = U.row0 + t * BM;
@@ -198,7 +205,7 @@ __device__ __forceinline__ Unit decode_unit(int u, const FwdParams& P) {
     U.n[t] = n;
   }
   U.nmax = max(U.n[0], U.n[1]);
-  return U;
+  return true;
 }
 
 struct Ctl {
@@ -295,9 +302,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, qit = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
-        const Unit U = decode_unit(u, P);
-        if (U.nmax == 0) continue;
+      for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+        Unit U;
+        if (!decode_unit(u >> 1, u & 1, P, U) || U.nmax == 0) continue;
         if (!wait_bounded(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
         const int nq = (U.n[0] > 0) + (U.n[1] > 0);
         mbar_arrive_expect_tx(BAR_Q_FULL, nq * C::Q_TILE_BYTES);
@@ -356,9 +363,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                          kv_smem + slot * C::KV_TILE_BYTES, acc);
       };
 
-      for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
-        const Unit U = decode_unit(u, P);
-        if (U.nmax == 0) continue;
+      for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+        Unit U;
+        if (!decode_unit(u >> 1, u & 1, P, U) || U.nmax == 0) continue;
         if (!wait_bounded(BAR_Q_FULL, qit & 1u, ctl, P)) { ok = false; break; }
         tc_fence_after();
         {
@@ -427,8 +434,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t sc = 0, oc = 0;  // phase counters of s_full[t], o_full[t]
     bool ok = true;
 
-    for (int u = blockIdx.x; ok && u < P.num_units; u += gridDim.x) {
-      const Unit U = decode_unit(u, P);
+    for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+      Unit U;
+      if (!decode_unit(u >> 1, u & 1, P, U)) continue;
       const int tile_row0 = U.row0 + t * BM;
       if (tile_row0 >= P.Sq) continue;  // idle tile
       const int row = tile_row0 + rloc;
@@ -459,13 +467,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
 
+        // all four 32-column loads in flight, one wait
         float s[BN];
+        {
+          uint32_t r0[32], r1[32], r2[32], r3[32];
+          tmem_ld32_async(t_lane + col_s + 0, r0);
+          tmem_ld32_async(t_lane + col_s + 32, r1);
+          tmem_ld32_async(t_lane + col_s + 64, r2);
+          tmem_ld32_async(t_lane + col_s + 96, r3);
+          tmem_ld_wait();
+          reg_fence(r0);
+          reg_fence(r1);
+          reg_fence(r2);
+          reg_fence(r3);
 #pragma unroll
-        for (int i = 0; i < BN / 32; ++i) {
-          uint32_t r[32];
-          tmem_ld32(t_lane + col_s + 32 * i, r);
-#pragma unroll
-          for (int c = 0; c < 32; ++c) s[32 * i + c] = __uint_as_float(r[c]);
+          for (int c = 0; c < 32; ++c) {
+            s[c] = __uint_as_float(r0[c]);
+            s[32 + c] = __uint_as_float(r1[c]);
+            s[64 + c] = __uint_as_float(r2[c]);
+            s[96 + c] = __uint_as_float(r3[c]);
+          }
         }
         // mask: keys past Sk, and (causal) keys after row + Sk - Sq
         int vis = P.Sk - j * BN;
