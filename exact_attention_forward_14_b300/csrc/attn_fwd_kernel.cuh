@@ -61,6 +61,10 @@ constexpr int NUM_THREADS = 320;
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
 constexpr float RESCALE_LOG2 = 8.0f;
+// FP8: P is written as p * 2^P_SCALE_LOG2 * (V block scale / largest V block
+// scale), so with p <= 2^4 the largest value is 256 and the lo part of the
+// split stays clear of the E4M3 subnormal range for every weight that matters.
+constexpr float P_SCALE_LOG2 = 4.0f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr int STATUS_TIMEOUT = 5;  // ATTN_ERR_TIMEOUT
 constexpr int FP8_BLOCK = 64;      // rows per FP8 scale block
@@ -99,8 +103,15 @@ struct Cfg {
   static constexpr int MMA_K = FP8 ? 32 : 16;  // 32 bytes of K per instruction
   static constexpr int KSTEPS_QK = D / MMA_K;
   static constexpr int KSTEPS_PV = BN / MMA_K;
-  static constexpr int P_COLS = BN * ESZ / 4;  // TMEM columns holding P
+  static constexpr int P_COLS = BN * ESZ / 4;  // TMEM columns holding one P part
   static constexpr int P_COLS_PER_KSTEP = MMA_K * ESZ / 4;
+  // FP8 keeps P to about 8 significant bits as two E4M3 parts (hi, lo), each
+  // multiplied by the same V tile; bf16 P is one part.
+  static constexpr int P_PARTS = FP8 ? 2 : 1;
+  // Stale-max threshold (log2 units): p <= 2^RESCALE before any scaling. FP8
+  // uses a lower one so p * P_SCALE stays inside the E4M3 range (<= 448).
+  static constexpr float RESCALE = FP8 ? 4.0f : RESCALE_LOG2;
+  static_assert(P_PARTS * P_COLS <= BN, "P parts must fit in the S columns");
   static constexpr uint32_t AB_FMT = FP8 ? 0u : 1u;  // e4m3 : bf16
   static constexpr uint32_t IDESC_S = make_idesc(BM, BN, AB_FMT, false);
   static constexpr uint32_t IDESC_PV = make_idesc(BM, D, AB_FMT, true);
@@ -144,7 +155,8 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O (+)= P V: P (128 x 128 keys) in tensor memory, packed along the keys;
+// O (+)= P V: P (128 x 128 keys) in tensor memory, packed along the keys
+// (FP8: the hi part in the first P_COLS columns, the lo part after it);
 // V tile staged by TMA with d contiguous (MN-major B operand): the leading
 // byte offset steps between d-chunks, the stride byte offset between groups
 // of 8 keys; each instruction consumes MMA_K keys.
@@ -153,13 +165,16 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
                                          bool accumulate) {
   using C = Cfg<D, FP8>;
 #pragma unroll
-  for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
-    const uint64_t b = make_sdesc(v_smem + ks * C::MMA_K * C::CHUNK_BYTES, C::KV_CHUNK_BYTES,
-                                  8 * C::CHUNK_BYTES, C::SWZ_CODE);
-    const uint32_t a = p_tmem + ks * C::P_COLS_PER_KSTEP;
-    const uint32_t acc = (accumulate || ks > 0) ? 1u : 0u;
-    if constexpr (FP8) mma_f8_ts(d_tmem, a, b, C::IDESC_PV, acc);
-    else mma_f16_ts(d_tmem, a, b, C::IDESC_PV, acc);
+  for (int part = 0; part < C::P_PARTS; ++part) {
+#pragma unroll
+    for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
+      const uint64_t b = make_sdesc(v_smem + ks * C::MMA_K * C::CHUNK_BYTES, C::KV_CHUNK_BYTES,
+                                    8 * C::CHUNK_BYTES, C::SWZ_CODE);
+      const uint32_t a = p_tmem + part * C::P_COLS + ks * C::P_COLS_PER_KSTEP;
+      const uint32_t acc = (accumulate || part > 0 || ks > 0) ? 1u : 0u;
+      if constexpr (FP8) mma_f8_ts(d_tmem, a, b, C::IDESC_PV, acc);
+      else mma_f16_ts(d_tmem, a, b, C::IDESC_PV, acc);
+    }
   }
 }
 
@@ -496,14 +511,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int c = 0; c < BN; ++c)
             if (c >= vis) s[c] = -INFINITY;
         }
-        // per-column-half exponent scales
-        float c_lo = cq, c_hi = cq, r_lo = 1.f, r_hi = 1.f;
+        // per-column-half exponent scales. FP8: the first and second 64 keys
+        // of the tile are two scale blocks of K and of V; e_* = log2 of the
+        // factor p is multiplied by before rounding to E4M3, inv_* = 1 / that
+        // factor (2^-P_SCALE_LOG2 * largest V scale / V block scale).
+        float c_lo = cq, c_hi = cq;
+        float e_lo = P_SCALE_LOG2, e_hi = P_SCALE_LOG2;
+        float inv_lo = 1.f / (1 << static_cast<int>(P_SCALE_LOG2)), inv_hi = inv_lo;
         if (FP8 && ks_row != nullptr) {
           const int kb0 = 2 * j, kb1 = 2 * j + 1;
+          const float vs0 = vs_row[kb0];
+          const float vs1 = kb1 < nblk_k ? vs_row[kb1] : v_ref;
           c_lo = cq * ks_row[kb0];
           c_hi = cq * (kb1 < nblk_k ? ks_row[kb1] : 1.f);
-          r_lo = vs_row[kb0] / v_ref;
-          r_hi = (kb1 < nblk_k ? vs_row[kb1] : v_ref) / v_ref;
+          e_lo = P_SCALE_LOG2 + __log2f(vs0 / v_ref);
+          e_hi = P_SCALE_LOG2 + __log2f(vs1 / v_ref);
+          inv_lo = v_ref / (vs0 * (1 << static_cast<int>(P_SCALE_LOG2)));
+          inv_hi = v_ref / (vs1 * (1 << static_cast<int>(P_SCALE_LOG2)));
         }
         // tile row max (in log2 units)
         float mx_lo = s[0], mx_hi = s[BN / 2];
@@ -525,7 +549,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         const float m_tile = fmaxf(mx_lo * c_lo, mx_hi * c_hi);
         const float m_new = fmaxf(m_run, m_tile);
-        const bool need = (m_new - m_run) > RESCALE_LOG2;  // false when both are -inf
+        const bool need = (m_new - m_run) > C::RESCALE;  // false when both are -inf
         float factor = 1.f;
         if (need) {
           factor = ex2_approx(m_run - m_new);
@@ -555,22 +579,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tmem_st32(t_lane + col_s + 32 * i, pk);
           }
         } else {
-          uint32_t pk[BN / 4];
+          // p' = p * rr * 2^P_SCALE_LOG2, the factor folded into the exponent;
+          // each 64-key half (one scale block) sums its p' separately and is
+          // divided back below. One half at a time: 16 columns of each part.
 #pragma unroll
-          for (int c = 0; c < BN / 4; ++c) {
-            const bool lo = 4 * c < BN / 2;
-            const float cc = lo ? c_lo : c_hi;
-            const float rr = lo ? r_lo : r_hi;
-            const float p0 = ex2_approx(fmaf(s[4 * c], cc, -msafe));
-            const float p1 = ex2_approx(fmaf(s[4 * c + 1], cc, -msafe));
-            const float p2 = ex2_approx(fmaf(s[4 * c + 2], cc, -msafe));
-            const float p3 = ex2_approx(fmaf(s[4 * c + 3], cc, -msafe));
-            l0 += p0; l1 += p1; l2 += p2; l3 += p3;
-            pk[c] = pack_e4m3x4(p0 * rr, p1 * rr, p2 * rr, p3 * rr);
+          for (int i = 0; i < 2; ++i) {
+            const float cc = i ? c_hi : c_lo;
+            const float off = (i ? e_hi : e_lo) - msafe;
+            uint32_t phi[16], plo[16];
+            float la = 0.f, lb = 0.f;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+              const int e = 64 * i + 4 * c;
+              const float p0 = ex2_approx(fmaf(s[e], cc, off));
+              const float p1 = ex2_approx(fmaf(s[e + 1], cc, off));
+              const float p2 = ex2_approx(fmaf(s[e + 2], cc, off));
+              const float p3 = ex2_approx(fmaf(s[e + 3], cc, off));
+              la += p0 + p2;
+              lb += p1 + p3;
+              split_e4m3x4(p0, p1, p2, p3, phi[c], plo[c]);
+            }
+            tmem_st16(t_lane + col_s + 16 * i, phi);
+            tmem_st16(t_lane + col_s + C::P_COLS + 16 * i, plo);
+            if (i == 0) { l0 = la; l1 = lb; } else { l2 = la; l3 = lb; }
           }
-          tmem_st32(t_lane + col_s, pk);
         }
-        l_run += (l0 + l1) + (l2 + l3);
+        if constexpr (FP8) l_run += (l0 + l1) * inv_lo + (l2 + l3) * inv_hi;
+        else l_run += (l0 + l1) + (l2 + l3);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
           // O_t holds the sum over earlier tiles: S_t(j) completing implies
           // the previous O_t += P V has completed as well. Done after P is
@@ -599,7 +634,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++oc;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
-        const float inv = l_run > 0.f ? v_ref / l_run : 0.f;
+        // FP8: O holds sum p * 2^P_SCALE_LOG2 * (V block scale / v_ref) * code
+        const float inv =
+            l_run > 0.f ? v_ref / (FP8 ? l_run * (1 << static_cast<int>(P_SCALE_LOG2)) : l_run)
+                        : 0.f;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t r[32];

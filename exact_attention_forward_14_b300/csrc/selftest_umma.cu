@@ -8,7 +8,10 @@
 //                  TMA K-major (the S = Q K^T step);
 //   form 1 ("PV"): D[128 x d]   = A[128 x 128] * B[128 x d], A written to
 //                  tensor memory by the threads (the P operand), B staged by
-//                  TMA with d contiguous (the O += P V step).
+//                  TMA with d contiguous (the O += P V step). For E4M3, A is
+//                  given as two parts (128 x 256 bytes: hi codes, then lo
+//                  codes, per row) and D = (hi + lo) * B, as the kernel's
+//                  split P is consumed.
 // d = 128; element type bf16 or E4M3. D is returned as fp32 row-major.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -84,11 +87,15 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         tmem_st32(t_lane + 128 + 32 * i, pk);
       }
     } else {
-      const uint32_t* ar = reinterpret_cast<const uint32_t*>(a_raw + row * 128);
-      uint32_t pk[32];
+      // two parts (hi, lo) of 128 E4M3 codes each; the MMA sums both
+      const uint32_t* ar = reinterpret_cast<const uint32_t*>(a_raw + row * 256);
 #pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = ar[c];  // four E4M3 codes, first key in bits 0..7
-      tmem_st32(t_lane + 128, pk);
+      for (int part = 0; part < 2; ++part) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) pk[c] = ar[32 * part + c];  // first key in bits 0..7
+        tmem_st32(t_lane + 128 + C::P_COLS * part, pk);
+      }
     }
     tmem_st_wait();
   }
@@ -160,8 +167,9 @@ int run_selftest(const void* a, const void* b, float* out, int* err, cudaStream_
 extern "C" {
 
 // form: 0 = QK form, 1 = PV form; fp8: 0 = bf16, 1 = E4M3. a, b: device,
-// 128 x 128 row-major; out: device fp32 128 x 128; err: device int set to 1
-// if a wait timed out. Returns an attn_status_t.
+// 128 x 128 row-major (a: 128 x 256 bytes for the E4M3 PV form); out: device
+// fp32 128 x 128; err: device int set to 1 if a wait timed out. Returns an
+// attn_status_t.
 int attn_selftest_umma(int form, int fp8, const void* a, const void* b, float* out, int* err,
                        attn_stream_t stream) {
   int dev = 0, major = 0, minor = 0;

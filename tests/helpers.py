@@ -10,12 +10,14 @@ def require_gpu():
     return torch
 
 
-def bf16_atol(ref):
-    """Per-element bound for bf16 O: max(1e-2, one bf16 ulp of the reference).
-    The output rounding alone is half an ulp, which exceeds 1e-2 once |O| >= 4."""
+def bf16_atol(ref, floor=1e-2):
+    """Per-element bound on O: max(floor, one bf16 ulp of the reference).
+    O is written as bf16, so its rounding alone is half an ulp, which exceeds
+    1e-2 once |O| >= 4 (and 6e-2 once |O| >= 16, reached with the FP8
+    workload's x20 outliers in V)."""
     ref = np.abs(np.asarray(ref, dtype=np.float64))
     e = np.floor(np.log2(np.maximum(ref, 1e-30)))
-    return np.maximum(1e-2, np.exp2(e - 7))
+    return np.maximum(floor, np.exp2(e - 7))
 
 
 def assert_o_close(o_gpu, o_ref, kind="bf16"):
@@ -23,10 +25,7 @@ def assert_o_close(o_gpu, o_ref, kind="bf16"):
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert np.isfinite(o_gpu).all(), "non-finite output"
     err = np.abs(o_gpu - o_ref)
-    if kind == "bf16":
-        tol = bf16_atol(o_ref)
-    else:
-        tol = np.full_like(o_ref, 6e-2)
+    tol = bf16_atol(o_ref, 1e-2 if kind == "bf16" else 6e-2)
     bad = err > tol
     assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside tolerance; "
                            f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")

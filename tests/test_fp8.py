@@ -65,7 +65,7 @@ def test_fp8_attention_small(oracle_mod, shape):
     q, k, v = inputs.draw_qkv_f32(B, Hq, Hkv, Sq, Sk, d, seed=sum(shape), outlier_frac=0.001)
     o, lse, o_ref, lse_ref = _fp8_case(oracle_mod, torch, q, k, v, causal, 1 / np.sqrt(d))
     assert_o_close(o.float().cpu().numpy(), o_ref, kind="fp8")
-    assert_lse_close(lse.cpu().numpy(), lse_ref, tol=1e-2)
+    assert_lse_close(lse.cpu().numpy(), lse_ref, tol=1e-3)
 
 
 @pytest.mark.gpu
@@ -79,4 +79,4 @@ def test_fp8_workload_sampled_rows(oracle_mod):
     h, i = np.divmod(rem, w.Sq)
     o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
     assert_o_close(o_g, o_ref, kind="fp8")
-    assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref, tol=1e-2)
+    assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref, tol=1e-3)
