@@ -37,7 +37,7 @@ DEFAULT_WORKLOAD = "b2h32s8192d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
                   "exact_attention_forward_14_b300/csrc/ptx.cuh"]
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+PROFILES = os.path.join(ROOT, "profiles")
 
 
 def kernel_source_hash() -> str:
@@ -57,81 +57,101 @@ def load_peaks():
 
 
 def ncu_traffic(workload: str):
-    """DRAM bytes per launch from a committed ncu capture, only while the
-    kernel sources still match the capture."""
-    if not os.path.exists(TRAFFIC_FILE):
-        return None
-    with open(TRAFFIC_FILE) as f:
-        t = json.load(f)
-    entry = t.get(workload)
-    if not entry or entry.get("kernel_hash") != kernel_source_hash():
-        return None
-    return entry.get("dram_bytes_per_launch")
+    """DRAM bytes per launch from the JSON block of a committed ncu summary
+    (profiles/*.md), only while the kernel sources still match the capture."""
+    import glob
+    import re
+    want = kernel_source_hash()
+    for path in sorted(glob.glob(os.path.join(PROFILES, "*.md"))):
+        with open(path) as f:
+            text = f.read()
+        for block in re.findall(r"```json\n(.*?)```", text, flags=re.S):
+            try:
+                entry = json.loads(block)
+            except ValueError:
+                continue
+            if entry.get("workload") == workload and entry.get("kernel_hash") == want:
+                return entry.get("dram_bytes_per_launch")
+    return None
 
 
 class ClockSampler:
-    """Samples SM clock and throttle reasons through NVML in a thread."""
+    """Samples SM clock, power and throttle reasons with ``nvidia-smi -lms``
+    in a background reader while the timed region runs. Only samples that
+    arrive between enter() and exit() are kept."""
 
-    REASONS = {
-        "gpu_idle": 0x1, "applications_clocks_setting": 0x2, "sw_power_cap": 0x4,
-        "hw_slowdown": 0x8, "sync_boost": 0x10, "sw_thermal_slowdown": 0x20,
-        "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80,
-        "display_clock_setting": 0x100,
-    }
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    FLAGS = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
-    def __init__(self, device_index: int, period_s: float = 0.005):
-        self.period = period_s
-        self.samples = []
-        self.reasons = set()
-        self.max_mhz = None
+    def __init__(self, device_index: int, period_ms: int = 20):
+        self.period_ms = period_ms
+        self.rows = []
         self.error = None
-        self._stop = threading.Event()
+        self._proc = None
         self._thread = None
-        try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nvml = pynvml
-            # NVML numbers devices physically; honour CUDA_VISIBLE_DEVICES
-            vis = os.environ.get("CUDA_VISIBLE_DEVICES")
-            idx = device_index
-            if vis and vis.split(",")[device_index].strip().isdigit():
-                idx = int(vis.split(",")[device_index])
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(idx)
-            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM)
-            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
-                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
-        except Exception as e:  # no NVML: report no clocks, say why
-            self._nvml = None
-            self.error = f"{type(e).__name__}: {e}"
+        self._active = False
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        self.index = device_index
+        if vis and vis.split(",")[device_index].strip().isdigit():
+            self.index = int(vis.split(",")[device_index])
 
-    def _run(self):
-        nv = self._nvml
-        while not self._stop.is_set():
-            try:
-                self.samples.append(nv.nvmlDeviceGetClockInfo(self._h, nv.NVML_CLOCK_SM))
-                mask = self._reasons_fn(self._h)
-                for name, bit in self.REASONS.items():
-                    if mask & bit and name != "gpu_idle":
-                        self.reasons.add(name)
-            except Exception as e:
-                self.error = f"{type(e).__name__}: {e}"
-            time.sleep(self.period)
+    def _reader(self):
+        for line in self._proc.stdout:
+            if self._active:
+                self.rows.append(line.strip())
+
+    def start(self):
+        """Starts nvidia-smi and returns once its first line has arrived."""
+        import subprocess
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}", f"-i={self.index}"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            first = self._proc.stdout.readline()
+            if not first:
+                raise RuntimeError("nvidia-smi printed nothing")
+        except Exception as e:
+            self.error = f"{type(e).__name__}: {e}"
+            self._proc = None
+            return self
+        self._thread = threading.Thread(target=self._reader, daemon=True)
+        self._thread.start()
+        return self
 
     def __enter__(self):
-        if self._nvml is not None:
-            self._thread = threading.Thread(target=self._run, daemon=True)
-            self._thread.start()
+        self._active = True
         return self
 
     def __exit__(self, *exc):
-        self._stop.set()
-        if self._thread is not None:
-            self._thread.join()
+        self._active = False
+        if self._proc is not None:
+            self._proc.terminate()
+            self._proc.wait()
+            self._thread.join(timeout=2)
 
     def summary(self):
-        out = {"sm_mhz": statistics.median(self.samples) if self.samples else None,
-               "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
-               "samples": len(self.samples), "source": "nvml"}
+        mhz, maxes, watts, reasons = [], [], [], set()
+        for r in self.rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                mhz.append(float(f[0]))
+                maxes.append(float(f[1]))
+                watts.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.FLAGS, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        out = {"sm_mhz": statistics.median(mhz) if mhz else None,
+               "sm_max_mhz": max(maxes) if maxes else None,
+               "power_w_max": max(watts) if watts else None,
+               "reasons": sorted(reasons), "samples": len(mhz),
+               "source": f"nvidia-smi -lms {self.period_ms}"}
         if self.error:
             out["error"] = self.error
         return out
@@ -282,7 +302,8 @@ def run_ours(args, w):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clocks:
+    clocks = ClockSampler(local).start()
+    with clocks:
         t0.record(stream)
         for a, b in ev:
             a.record(stream)
@@ -379,7 +400,7 @@ def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__,
                                  formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
