@@ -123,8 +123,8 @@ struct Cfg {
   static constexpr int OFF_KV = 2 * Q_TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_TILE_BYTES;
   // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
-  // p_full[2], o_full[2], drain
-  static constexpr int NUM_BARS = 2 + 2 * NSLOT + 7;
+  // p_full[2 tiles][2 halves], o_full[2], drain
+  static constexpr int NUM_BARS = 2 + 2 * NSLOT + 9;
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // Launch with the whole opt-in budget (one CTA per SM either way), so a
@@ -155,19 +155,22 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
   }
 }
 
-// O (+)= P V: P (128 x 128 keys) in tensor memory, packed along the keys
-// (FP8: the hi part in the first P_COLS columns, the lo part after it);
-// V tile staged by TMA with d contiguous (MN-major B operand): the leading
-// byte offset steps between d-chunks, the stride byte offset between groups
-// of 8 keys; each instruction consumes MMA_K keys.
+// O (+)= P V for one half of the K/V tile (keys [64 h, 64 h + 64)): P
+// (128 x 128 keys) in tensor memory, packed along the keys (FP8: the hi part
+// in the first P_COLS columns, the lo part after it); V tile staged by TMA
+// with d contiguous (MN-major B operand): the leading byte offset steps
+// between d-chunks, the stride byte offset between groups of 8 keys; each
+// instruction consumes MMA_K keys. `accumulate` = false starts O afresh.
 template <int D, bool FP8>
-__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
-                                         bool accumulate) {
+__device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                              int half, bool accumulate) {
   using C = Cfg<D, FP8>;
+  constexpr int KS_HALF = C::KSTEPS_PV / 2;
 #pragma unroll
   for (int part = 0; part < C::P_PARTS; ++part) {
 #pragma unroll
-    for (int ks = 0; ks < C::KSTEPS_PV; ++ks) {
+    for (int k = 0; k < KS_HALF; ++k) {
+      const int ks = half * KS_HALF + k;
       const uint64_t b = make_sdesc(v_smem + ks * C::MMA_K * C::CHUNK_BYTES, C::KV_CHUNK_BYTES,
                                     8 * C::CHUNK_BYTES, C::SWZ_CODE);
       const uint32_t a = p_tmem + part * C::P_COLS + ks * C::P_COLS_PER_KSTEP;
@@ -176,6 +179,14 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
       else mma_f16_ts(d_tmem, a, b, C::IDESC_PV, acc);
     }
   }
+}
+
+// Both halves (used by the single-tile self-test).
+template <int D, bool FP8>
+__device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+                                         bool accumulate) {
+  issue_pv_half<D, FP8>(d_tmem, p_tmem, v_smem, 0, accumulate);
+  issue_pv_half<D, FP8>(d_tmem, p_tmem, v_smem, 1, true);
 }
 
 struct Unit {
@@ -275,8 +286,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t BAR_KV_FULL = bar0 + 16;                     // + 8 * slot
   const uint32_t BAR_KV_EMPTY = BAR_KV_FULL + 8 * C::NSLOT;   // + 8 * slot
   const uint32_t BAR_S_FULL = BAR_KV_EMPTY + 8 * C::NSLOT;    // + 8 * t
-  const uint32_t BAR_P_FULL = BAR_S_FULL + 16;                // + 8 * t
-  const uint32_t BAR_O_FULL = BAR_P_FULL + 16;                // + 8 * t
+  const uint32_t BAR_P_FULL = BAR_S_FULL + 16;                // + 16 * t + 8 * half
+  const uint32_t BAR_O_FULL = BAR_P_FULL + 32;                // + 8 * t
   const uint32_t BAR_DRAIN = BAR_O_FULL + 16;
   volatile Ctl* ctl = reinterpret_cast<volatile Ctl*>(smem + C::OFF_MISC);
 
@@ -293,7 +304,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR_S_FULL + 8 * t, 1);
-      mbar_init(BAR_P_FULL + 8 * t, BM);
+      // one elected arrive per softmax warp; a barrier per P half, so each
+      // completes once per K/V tile and its parity cannot run ahead
+      mbar_init(BAR_P_FULL + 16 * t, BM / 32);
+      mbar_init(BAR_P_FULL + 16 * t + 8, BM / 32);
       mbar_init(BAR_O_FULL + 8 * t, 1);
     }
     mbar_init(BAR_DRAIN, 1);
@@ -373,9 +387,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issue_qk<D, FP8>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
                          kv_smem + slot * C::KV_TILE_BYTES);
       };
-      auto issue_o = [&](int t, uint32_t slot, bool acc) {
-        issue_pv<D, FP8>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
-                         kv_smem + slot * C::KV_TILE_BYTES, acc);
+      auto issue_o = [&](int t, uint32_t slot, int half, bool acc) {
+        issue_pv_half<D, FP8>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
+                              kv_smem + slot * C::KV_TILE_BYTES, half, acc);
       };
 
       for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
@@ -405,10 +419,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
             if (j < U.n[t]) {
-              if (!wait_bounded(BAR_P_FULL + 8 * t, pc[t] & 1u, ctl, P)) { ok = false; break; }
+              // P arrives in two halves of 64 keys, one barrier each
+              for (int h = 0; ok && h < 2; ++h) {
+                if (!wait_bounded(BAR_P_FULL + 16 * t + 8 * h, pc[t] & 1u, ctl, P)) { ok = false; break; }
+                tc_fence_after();
+                issue_o(t, vslot, h, j > 0);
+              }
+              if (!ok) break;
               ++pc[t];
-              tc_fence_after();
-              issue_o(t, vslot, j > 0);
               if (j == U.n[t] - 1) tc_commit(BAR_O_FULL + 8 * t);
             }
             if (t == 0 && more) {
@@ -529,25 +547,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           inv_lo = v_ref / (vs0 * (1 << static_cast<int>(P_SCALE_LOG2)));
           inv_hi = v_ref / (vs1 * (1 << static_cast<int>(P_SCALE_LOG2)));
         }
-        // tile row max (in log2 units)
-        float mx_lo = s[0], mx_hi = s[BN / 2];
-        {
-          float a0 = s[0], a1 = s[1], a2 = s[2], a3 = s[3];
+        // row max of each 64-key half (raw scores; the exponent scale of a
+        // half is positive, so it commutes with the max)
+        float mx[2];
 #pragma unroll
-          for (int c = 4; c < BN / 2; c += 4) {
-            a0 = fmaxf(a0, s[c]); a1 = fmaxf(a1, s[c + 1]);
-            a2 = fmaxf(a2, s[c + 2]); a3 = fmaxf(a3, s[c + 3]);
-          }
-          mx_lo = fmaxf(fmaxf(a0, a1), fmaxf(a2, a3));
-          float b0 = s[BN / 2], b1 = s[BN / 2 + 1], b2 = s[BN / 2 + 2], b3 = s[BN / 2 + 3];
+        for (int i = 0; i < 2; ++i) {
+          const float* h = s + 64 * i;
+          float a0 = h[0], a1 = h[1], a2 = h[2], a3 = h[3];
 #pragma unroll
-          for (int c = BN / 2 + 4; c < BN; c += 4) {
-            b0 = fmaxf(b0, s[c]); b1 = fmaxf(b1, s[c + 1]);
-            b2 = fmaxf(b2, s[c + 2]); b3 = fmaxf(b3, s[c + 3]);
+          for (int c = 4; c < 60; c += 8) {
+            a0 = max3(a0, h[c], h[c + 1]);
+            a1 = max3(a1, h[c + 2], h[c + 3]);
+            a2 = max3(a2, h[c + 4], h[c + 5]);
+            a3 = max3(a3, h[c + 6], h[c + 7]);
           }
-          mx_hi = fmaxf(fmaxf(b0, b1), fmaxf(b2, b3));
+          a0 = max3(a0, h[60], h[61]);
+          a1 = max3(a1, h[62], h[63]);
+          mx[i] = fmaxf(max3(a0, a1, a2), a3);
         }
-        const float m_tile = fmaxf(mx_lo * c_lo, mx_hi * c_hi);
+        const float m_tile = fmaxf(mx[0] * c_lo, mx[1] * c_hi);
         const float m_new = fmaxf(m_run, m_tile);
         const bool need = (m_new - m_run) > C::RESCALE;  // false when both are -inf
         float factor = 1.f;
@@ -557,71 +575,74 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           m_run = m_new;
         }
         const float msafe = (m_run == -INFINITY) ? 0.f : m_run;
-        float l0 = 0.f, l1 = 0.f, l2 = 0.f, l3 = 0.f;
-        if constexpr (!FP8) {
-          // 64 keys -> 32 packed columns per store, so the P registers of one
-          // half are free before the next half is computed
+        // O_t holds the sum over earlier tiles (S_t(j) completing implies the
+        // previous O_t += P V has completed too); it is rescaled before the
+        // first half of P is handed over, after that half's registers are free.
+        const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
+
+        // p = 2^(s * c - m): paired fp32 FMA, one MUFU ex2 per key, paired
+        // sums. FP8: p' = p * rr * 2^P_SCALE_LOG2 with log2(rr * 2^P_SCALE_LOG2)
+        // folded into the offset; each half sums its p' separately and is
+        // divided back when added to l.
 #pragma unroll
-          for (int i = 0; i < BN / 64; ++i) {
-            const float cc = (i < BN / 128) ? c_lo : c_hi;
+        for (int i = 0; i < 2; ++i) {
+          const float cc = i ? c_hi : c_lo;
+          const float off = (FP8 ? (i ? e_hi : e_lo) : 0.f) - msafe;
+          const uint64_t cc2 = f2_pack(cc, cc), off2 = f2_pack(off, off);
+          uint64_t acc0 = 0ull, acc1 = 0ull;  // (+0, +0) pairs
+          const float* h = s + 64 * i;
+          if constexpr (!FP8) {
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-              const int e = 64 * i + 2 * c;
-              const float p0 = ex2_approx(fmaf(s[e], cc, -msafe));
-              const float p1 = ex2_approx(fmaf(s[e + 1], cc, -msafe));
-              const float p2 = ex2_approx(fmaf(s[e + 2], cc, -msafe));
-              const float p3 = ex2_approx(fmaf(s[e + 3], cc, -msafe));
-              l0 += p0; l1 += p1; l2 += p2; l3 += p3;
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(h[2 * c], h[2 * c + 1]), cc2, off2), x0, x1);
+              f2_unpack(f2_fma(f2_pack(h[2 * c + 2], h[2 * c + 3]), cc2, off2), x2, x3);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+              acc1 = f2_add(acc1, f2_pack(p2, p3));
               pk[c] = pack_bf16x2(p0, p1);
               pk[c + 1] = pack_bf16x2(p2, p3);
             }
             tmem_st32(t_lane + col_s + 32 * i, pk);
-          }
-        } else {
-          // p' = p * rr * 2^P_SCALE_LOG2, the factor folded into the exponent;
-          // each 64-key half (one scale block) sums its p' separately and is
-          // divided back below. One half at a time: 16 columns of each part.
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const float cc = i ? c_hi : c_lo;
-            const float off = (i ? e_hi : e_lo) - msafe;
+          } else {
             uint32_t phi[16], plo[16];
-            float la = 0.f, lb = 0.f;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
-              const int e = 64 * i + 4 * c;
-              const float p0 = ex2_approx(fmaf(s[e], cc, off));
-              const float p1 = ex2_approx(fmaf(s[e + 1], cc, off));
-              const float p2 = ex2_approx(fmaf(s[e + 2], cc, off));
-              const float p3 = ex2_approx(fmaf(s[e + 3], cc, off));
-              la += p0 + p2;
-              lb += p1 + p3;
+              float x0, x1, x2, x3;
+              f2_unpack(f2_fma(f2_pack(h[4 * c], h[4 * c + 1]), cc2, off2), x0, x1);
+              f2_unpack(f2_fma(f2_pack(h[4 * c + 2], h[4 * c + 3]), cc2, off2), x2, x3);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
+              acc0 = f2_add(acc0, f2_pack(p0, p1));
+              acc1 = f2_add(acc1, f2_pack(p2, p3));
               split_e4m3x4(p0, p1, p2, p3, phi[c], plo[c]);
             }
             tmem_st16(t_lane + col_s + 16 * i, phi);
             tmem_st16(t_lane + col_s + C::P_COLS + 16 * i, plo);
-            if (i == 0) { l0 = la; l1 = lb; } else { l2 = la; l3 = lb; }
           }
-        }
-        if constexpr (FP8) l_run += (l0 + l1) * inv_lo + (l2 + l3) * inv_hi;
-        else l_run += (l0 + l1) + (l2 + l3);
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
-          // O_t holds the sum over earlier tiles: S_t(j) completing implies
-          // the previous O_t += P V has completed as well. Done after P is
-          // written so the score registers are already free.
+          float q0, q1, q2, q3;
+          f2_unpack(acc0, q0, q1);
+          f2_unpack(acc1, q2, q3);
+          const float lsum = (q0 + q1) + (q2 + q3);
+          if constexpr (FP8) l_run += lsum * (i ? inv_hi : inv_lo);
+          else l_run += lsum;
+          if (i == 0 && rescale_o) {
 #pragma unroll
-          for (int i = 0; i < D / 32; ++i) {
-            uint32_t r[32];
-            tmem_ld32(t_lane + col_o + 32 * i, r);
+            for (int k = 0; k < D / 32; ++k) {
+              uint32_t r[32];
+              tmem_ld32(t_lane + col_o + 32 * k, r);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
-            tmem_st32(t_lane + col_o + 32 * i, r);
+              for (int c = 0; c < 32; ++c) r[c] = __float_as_uint(__uint_as_float(r[c]) * factor);
+              tmem_st32(t_lane + col_o + 32 * k, r);
+            }
           }
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(BAR_P_FULL + 16 * t + 8 * i);
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(BAR_P_FULL + 8 * t);
       }
       if (!ok) break;
 
