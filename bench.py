@@ -160,11 +160,19 @@ class ClockSampler:
 # ------------------------------------------------------------ CPU oracle --
 
 def _oracle_inputs(w):
-    """The workload's inputs as raw bits for the oracle (drawn once)."""
+    """The workload's inputs in the oracle's form (drawn once): bf16 bits, or
+    for the FP8 workload E4M3 codes and block scales from the oracle's own
+    quantiser."""
     os.environ.setdefault("OMP_NUM_THREADS", str(len(os.sched_getaffinity(0))))
+    import oracle
     from exact_attention_forward_14_b300 import inputs
+    if w.dtype == "e4m3":
+        qc, kc, vc = (oracle.quantize_fp8_e4m3(t.numpy()) for t in inputs.draw_workload_f32(w))
+        return {"dtype": "e4m3", "q": qc[0], "k": kc[0], "v": vc[0],
+                "q_scale": qc[1], "k_scale": kc[1], "v_scale": vc[1]}
     q, k, v = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
-    return tuple(inputs.bf16_bits(t) for t in (q, k, v))
+    return {"dtype": "bf16", "q": inputs.bf16_bits(q), "k": inputs.bf16_bits(k),
+            "v": inputs.bf16_bits(v)}
 
 
 def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = None):
@@ -173,7 +181,6 @@ def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = No
     Returns (flops_of_sample, seconds, n_rows, threads)."""
     import numpy as np
     import oracle
-    qb, kb, vb = bits
 
     def rows_flops(rows):
         i = rows % w.Sq
@@ -189,7 +196,9 @@ def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = No
     while True:
         rows = np.sort(rng.choice(total, size=min(n, total), replace=False)).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.attn_fwd(qb, kb, vb, w.causal, w.scale, rows=rows)
+        oracle.attn_fwd(bits["q"], bits["k"], bits["v"], w.causal, w.scale, dtype=bits["dtype"],
+                        q_scale=bits.get("q_scale"), k_scale=bits.get("k_scale"),
+                        v_scale=bits.get("v_scale"), rows=rows)
         dt = time.perf_counter() - t0
         if n_fixed or dt >= target_s or n >= total:
             return rows_flops(rows), dt, rows.size, int(os.environ["OMP_NUM_THREADS"])
@@ -239,6 +248,24 @@ def workload_config(w):
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
             "d": w.d, "causal": w.causal, "dtype": w.dtype,
             "l2": "inputs larger than L2 (no flush)"}
+
+
+# ------------------------------------------------------ rank arithmetic --
+
+def max_over_ranks(x: float, dist=None, device="cpu") -> float:
+    """The slowest rank's figure (every rank gets it); x itself with one rank."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(flops_per_step: float, steps: int, world: int, total_ms: float) -> float:
+    """Whole-job throughput: every rank ran `steps` steps of `flops_per_step`
+    in (at most) total_ms."""
+    return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
 # ------------------------------------------------------------- GPU path --
@@ -318,13 +345,10 @@ def run_ours(args, w):
         raise ea.AttnError(st, "timed region")
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    if dist is not None:
-        tt = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
+    total_ms = max_over_ranks(total_ms, dist, dev)
     ms_per_step = total_ms / args.steps
     flops = w.flops()
-    value = world * flops * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_tflops(flops, args.steps, world, total_ms)
 
     # end to end through the public API: pinned host inputs -> device -> kernel
     # -> O and LSE back to pinned host memory, every step
@@ -351,13 +375,10 @@ def run_ours(args, w):
         e1.record(stream)
         torch.cuda.synchronize(dev)
         e_ms = e0.elapsed_time(e1)
-        if dist is not None:
-            tt = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        e_ms = max_over_ranks(e_ms, dist, dev)
         h2d = sum(t.numel() * t.element_size() for t in host)
         d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": world * flops * e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e2e = {"value": job_tflops(flops, e_steps, world, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e_steps}
 

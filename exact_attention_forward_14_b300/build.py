@@ -3,8 +3,11 @@
     python -m exact_attention_forward_14_b300.build [--force] [--verbose]
 
 Produces, next to this file:
-  libattn_b300.so     the attention library (C ABI in include/attn_b300.h)
-  libattn_selftest.so single-tile tensor-core layout checks used by the tests
+  libattn_b300.so           the attention library (C ABI in include/attn_b300.h)
+  libattn_selftest.so       single-tile tensor-core layout checks used by the tests
+  libattn_watchdog_test.so  test-only build of the library whose Q barrier is
+                            never armed, so every launch ends through the
+                            watchdog (bounded wait -> ATTN_ERR_TIMEOUT)
 """
 from __future__ import annotations
 
@@ -27,9 +30,11 @@ NVCC_FLAGS = [
     "-I" + INCLUDE, "-I" + CSRC,
 ]
 
+# name -> (sources, extra nvcc flags)
 TARGETS = {
-    "libattn_b300.so": ["attn_api.cu"],
-    "libattn_selftest.so": ["selftest_umma.cu"],
+    "libattn_b300.so": (["attn_api.cu"], []),
+    "libattn_selftest.so": (["selftest_umma.cu"], []),
+    "libattn_watchdog_test.so": (["attn_api.cu"], ["-DATTN_TEST_NEVER_ARM_Q"]),
 }
 
 
@@ -51,12 +56,12 @@ def build(force: bool = False, verbose: bool = False) -> list[str]:
     deps = (glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(INCLUDE, "*.h"))
             + [os.path.abspath(__file__)])
     built = []
-    for name, srcs in TARGETS.items():
+    for name, (srcs, extra) in TARGETS.items():
         out = os.path.join(PKG, name)
         if not force and not _stale(out, deps):
             continue
         tmp = out + f".tmp{os.getpid()}"
-        cmd = [_nvcc(), *NVCC_FLAGS, *(["-Xptxas", "-v"] if verbose else []),
+        cmd = [_nvcc(), *NVCC_FLAGS, *extra, *(["-Xptxas", "-v"] if verbose else []),
                *[os.path.join(CSRC, s) for s in srcs], "-o", tmp]
         if verbose:
             print(" ".join(cmd), flush=True)

@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         Unit U;
         if (!decode_unit(u >> 1, u & 1, P, U) || U.nmax == 0) continue;
         if (!wait_bounded(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
+#ifndef ATTN_TEST_NEVER_ARM_Q
         const int nq = (U.n[0] > 0) + (U.n[1] > 0);
         mbar_arrive_expect_tx(BAR_Q_FULL, nq * C::Q_TILE_BYTES);
 #pragma unroll
@@ -346,6 +347,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         BAR_Q_FULL, c * C::CHUNK_ELEMS, U.hq, U.row0 + t * BM, U.b);
         }
         ++qit;
+#endif
+        // (The watchdog test library is built with ATTN_TEST_NEVER_ARM_Q: Q is
+        // never loaded and q_full never completes, so the MMA warp's bounded
+        // wait runs out and the launch ends with ATTN_ERR_TIMEOUT.)
         for (int j = 0; ok && j < U.nmax; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {

@@ -39,6 +39,13 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_watchdog_test_library_exports_the_same_boundary(lib):
+    import ctypes
+    wd = ctypes.CDLL(os.path.join(PKG, "libattn_watchdog_test.so"))
+    for name in declared_functions():
+        assert hasattr(wd, name), name
+
+
 def test_status_strings(lib):
     names = {0: "ATTN_OK", 1: "ATTN_ERR_INVALID_ARG", 2: "ATTN_ERR_UNSUPPORTED",
              3: "ATTN_ERR_MISALIGNED", 4: "ATTN_ERR_CUDA", 5: "ATTN_ERR_TIMEOUT"}
