@@ -170,9 +170,9 @@ def _oracle_inputs(w):
         qc, kc, vc = (oracle.quantize_fp8_e4m3(t.numpy()) for t in inputs.draw_workload_f32(w))
         return {"dtype": "e4m3", "q": qc[0], "k": kc[0], "v": vc[0],
                 "q_scale": qc[1], "k_scale": kc[1], "v_scale": vc[1]}
-    q, k, v = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
-    return {"dtype": "bf16", "q": inputs.bf16_bits(q), "k": inputs.bf16_bits(k),
-            "v": inputs.bf16_bits(v)}
+    q, k, v = inputs.draw_workload_16(w)
+    return {"dtype": w.dtype, "q": inputs.bits16(q), "k": inputs.bits16(k),
+            "v": inputs.bits16(v)}
 
 
 def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = None):
@@ -296,10 +296,11 @@ def run_ours(args, w):
         dev_in = (q8, k8, v8, qs, ks, vs)
         del qf, kf, vf
     else:
-        hq, hk, hv = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
+        hq, hk, hv = inputs.draw_workload_16(w)
         host = tuple(t.pin_memory() for t in (hq, hk, hv))
         dev_in = tuple(t.to(dev) for t in host)
-    o = torch.empty((w.B, w.Sq, w.Hq, w.d), dtype=torch.bfloat16, device=dev)
+    o = torch.empty((w.B, w.Sq, w.Hq, w.d),
+                    dtype=torch.float16 if w.dtype == "f16" else torch.bfloat16, device=dev)
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -311,7 +312,7 @@ def run_ours(args, w):
         else:
             q, k, v = dev_in
             rc = ea.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal,
-                             w.scale, ea.ATTN_BF16, stream)
+                             w.scale, ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
         if rc != ea.ATTN_OK:
             raise ea.AttnError(rc, "attn_fwd")
 
@@ -394,7 +395,8 @@ def run_ours(args, w):
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-        "kernel": f"attn_fwd_kernel<{w.d},{'true' if w.dtype == 'e4m3' else 'false'}>",
+        "kernel": f"attn_fwd_kernel<{w.d},{str(w.dtype == 'e4m3').lower()},"
+                  f"{str(w.dtype == 'f16').lower()}>",
         "peak_source": (f"{peaks_src} bf16 burst" if w.dtype != "e4m3"
                         else f"{peaks_src} bf16 burst x 2 (nominal fp8/bf16 ratio)"),
         "frac_of_sustained": achieved / (peaks.get("bf16_tflops_sustained", peak) *
@@ -405,7 +407,7 @@ def run_ours(args, w):
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if w.dtype == "e4m3" else "bf16", "data": "synthetic",
+        "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w), "clocks": clocks.summary(), "e2e": e2e,
         "gpu_launches": args.steps, "roofline": roofline,
     }

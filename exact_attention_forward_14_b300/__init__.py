@@ -18,7 +18,7 @@ import threading
 
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
-    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "AttnError",
+    "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "ATTN_F16", "AttnError",
     "attn_fwd", "attn_fwd_fp8", "attn_quantize_fp8_e4m3", "attn_device_status",
     "attn_status_string", "forward", "forward_fp8", "quantize_fp8", "library_path", "load",
 ]
@@ -31,6 +31,7 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_TIMEOUT = 5
 ATTN_BF16 = 0
 ATTN_FP8_E4M3 = 1
+ATTN_F16 = 2
 FP8_BLOCK_ROWS = 64
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -133,21 +134,30 @@ def _check(rc, what):
 
 def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
             stream=None):
-    """bf16 attention forward. q [B,Sq,Hq,d], k/v [B,Sk,Hkv,d] (CUDA, contiguous).
-    Returns (o bf16 [B,Sq,Hq,d], lse fp32 [B,Hq,Sq])."""
+    """bf16 or fp16 attention forward. q [B,Sq,Hq,d], k/v [B,Sk,Hkv,d] (CUDA,
+    contiguous, all of one dtype). Returns (o [B,Sq,Hq,d] in the inputs'
+    dtype, lse fp32 [B,Hq,Sq])."""
     import torch
     B, Sq, Hq, d = q.shape
     _, Sk, Hkv, _ = k.shape
+    if q.dtype == torch.bfloat16:
+        code = ATTN_BF16
+    elif q.dtype == torch.float16:
+        code = ATTN_F16
+    else:
+        raise TypeError(f"forward takes bf16 or fp16 tensors, not {q.dtype}")
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
     if scale is None:
         scale = 1.0 / math.sqrt(d)
     if out is None:
-        out = torch.empty((B, Sq, Hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((B, Sq, Hq, d), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     for t in (q, k, v, out, lse):
         if not t.is_contiguous():
             raise ValueError("all tensors must be contiguous")
-    _check(attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, ATTN_BF16, stream),
+    _check(attn_fwd(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, code, stream),
            "attn_fwd")
     return out, lse
 

@@ -84,12 +84,12 @@ bool fits_i32(long long a, long long b, long long c, long long d) {
   return x <= lim;
 }
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16>
 int launch(const void* q, const void* k, const void* v, const float* qs, const float* ks,
            const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk,
            int causal, float scale, cudaStream_t stream, DeviceInfo* di, uint32_t attr_bit) {
-  using C = Cfg<D, FP8>;
-  auto kern = attnb3::attn_fwd_kernel<D, FP8>;
+  using C = Cfg<D, FP8, F16>;
+  auto kern = attnb3::attn_fwd_kernel<D, FP8, F16>;
   if (!(di->attr_done.load(std::memory_order_acquire) & attr_bit)) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
@@ -97,13 +97,13 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
     di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
   }
   CUtensorMap tq, tk, tv;
-  if (!encode_bshd(&tq, q, FP8, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BM) ||
-      !encode_bshd(&tk, k, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN) ||
-      !encode_bshd(&tv, v, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN))
+  if (!encode_bshd(&tq, q, FP8, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BM, F16) ||
+      !encode_bshd(&tk, k, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN, F16) ||
+      !encode_bshd(&tv, v, FP8, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BN, F16))
     return ATTN_ERR_CUDA;
 
   FwdParams P;
-  P.o = static_cast<__nv_bfloat16*>(o);
+  P.o = static_cast<uint16_t*>(o);
   P.lse = lse;
   P.q_scale = qs;
   P.k_scale = ks;
@@ -144,23 +144,29 @@ int check_attn_args(const void* q, const void* k, const void* v, void* o, float*
 
 int run_attn(const void* q, const void* k, const void* v, const float* qs, const float* ks,
              const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
-             int causal, float scale, bool fp8, cudaStream_t stream) {
+             int causal, float scale, bool fp8, bool f16, cudaStream_t stream) {
   DeviceInfo* di = nullptr;
   int rc = current_device(&di);
   if (rc != ATTN_OK) return rc;
   if (!get_encoder()) return ATTN_ERR_CUDA;
-  if (!fp8 && d == 128)
-    return launch<128, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
-                              stream, di, 1u);
-  if (!fp8 && d == 64)
-    return launch<64, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
-                             stream, di, 2u);
   if (fp8 && d == 128)
-    return launch<128, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
-                             stream, di, 4u);
+    return launch<128, true, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                    scale, stream, di, 4u);
   if (fp8 && d == 64)
-    return launch<64, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale,
-                            stream, di, 8u);
+    return launch<64, true, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                   scale, stream, di, 8u);
+  if (f16 && d == 128)
+    return launch<128, false, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                    scale, stream, di, 16u);
+  if (f16 && d == 64)
+    return launch<64, false, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                   scale, stream, di, 32u);
+  if (d == 128)
+    return launch<128, false, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                     scale, stream, di, 1u);
+  if (d == 64)
+    return launch<64, false, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
+                                    scale, stream, di, 2u);
   return ATTN_ERR_UNSUPPORTED;
 }
 
@@ -173,12 +179,12 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
              attn_stream_t stream) {
   int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
-  if (dtype == ATTN_BF16)
+  if (dtype == ATTN_BF16 || dtype == ATTN_F16)
     return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
-                    scale, false, reinterpret_cast<cudaStream_t>(stream));
+                    scale, false, dtype == ATTN_F16, reinterpret_cast<cudaStream_t>(stream));
   if (dtype == ATTN_FP8_E4M3)  // null scale pointers: every block scale is 1
     return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
-                    scale, true, reinterpret_cast<cudaStream_t>(stream));
+                    scale, true, false, reinterpret_cast<cudaStream_t>(stream));
   return ATTN_ERR_UNSUPPORTED;
 }
 
@@ -191,7 +197,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_sca
   if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
     return ATTN_ERR_MISALIGNED;
   return run_attn(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
-                  scale, true, reinterpret_cast<cudaStream_t>(stream));
+                  scale, true, false, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, int S, int H,

@@ -70,7 +70,7 @@ constexpr int STATUS_TIMEOUT = 5;  // ATTN_ERR_TIMEOUT
 constexpr int FP8_BLOCK = 64;      // rows per FP8 scale block
 
 struct FwdParams {
-  __nv_bfloat16* o;
+  uint16_t* o;           // bf16 or fp16 bits [B, Sq, Hq, d]
   float* lse;
   const float* q_scale;  // FP8 only: [B, Hq, ceil(Sq/64)]
   const float* k_scale;  // FP8 only: [B, Hkv, ceil(Sk/64)]
@@ -87,7 +87,7 @@ struct FwdParams {
   int* status;       // device status word
 };
 
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16 = false>
 struct Cfg {
   static constexpr int ESZ = FP8 ? 1 : 2;
   static constexpr int ROW_BYTES = D * ESZ;
@@ -112,7 +112,8 @@ struct Cfg {
   // uses a lower one so p * P_SCALE stays inside the E4M3 range (<= 448).
   static constexpr float RESCALE = FP8 ? 4.0f : RESCALE_LOG2;
   static_assert(P_PARTS * P_COLS <= BN, "P parts must fit in the S columns");
-  static constexpr uint32_t AB_FMT = FP8 ? 0u : 1u;  // e4m3 : bf16
+  // operand format: kind::f8f6f4 0 = e4m3; kind::f16 0 = f16, 1 = bf16
+  static constexpr uint32_t AB_FMT = (FP8 || F16) ? 0u : 1u;
   static constexpr uint32_t IDESC_S = make_idesc(BM, BN, AB_FMT, false);
   static constexpr uint32_t IDESC_PV = make_idesc(BM, D, AB_FMT, true);
   static constexpr int COL_S0 = 0;
@@ -138,9 +139,9 @@ struct Cfg {
 // S = Q K^T for one 128-row Q tile and one 128-key K tile, both staged by TMA
 // as K-major rows in 128-byte (or 64-byte) swizzled chunks of CHUNK_BYTES
 // columns; each instruction consumes 32 bytes of the head dimension.
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16 = false>
 __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, F16>;
 #pragma unroll
   for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
     const uint32_t byte_k = ks * 32;
@@ -161,10 +162,10 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 // with d contiguous (MN-major B operand): the leading byte offset steps
 // between d-chunks, the stride byte offset between groups of 8 keys; each
 // instruction consumes MMA_K keys. `accumulate` = false starts O afresh.
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16 = false>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                               int half, bool accumulate) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, F16>;
   constexpr int KS_HALF = C::KSTEPS_PV / 2;
 #pragma unroll
   for (int part = 0; part < C::P_PARTS; ++part) {
@@ -182,11 +183,11 @@ __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, 
 }
 
 // Both halves (used by the single-tile self-test).
-template <int D, bool FP8>
+template <int D, bool FP8, bool F16 = false>
 __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                          bool accumulate) {
-  issue_pv_half<D, FP8>(d_tmem, p_tmem, v_smem, 0, accumulate);
-  issue_pv_half<D, FP8>(d_tmem, p_tmem, v_smem, 1, true);
+  issue_pv_half<D, FP8, F16>(d_tmem, p_tmem, v_smem, 0, accumulate);
+  issue_pv_half<D, FP8, F16>(d_tmem, p_tmem, v_smem, 1, true);
 }
 
 struct Unit {
@@ -270,12 +271,15 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
   }
 }
 
-template <int D, bool FP8>
+// F16: q, k, v and o are fp16 (P is packed as f16 too); otherwise 16-bit
+// data is bf16 and FP8 inputs produce a bf16 O.
+template <int D, bool FP8, bool F16>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, F16>;
+  static_assert(!(FP8 && F16), "FP8 inputs give a bf16 O");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -389,11 +393,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t kv_smem = sbase + C::OFF_KV;
 
       auto issue_s = [&](int t, uint32_t slot) {
-        issue_qk<D, FP8>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
+        issue_qk<D, FP8, F16>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
                          kv_smem + slot * C::KV_TILE_BYTES);
       };
       auto issue_o = [&](int t, uint32_t slot, int half, bool acc) {
-        issue_pv_half<D, FP8>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
+        issue_pv_half<D, FP8, F16>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
                               kv_smem + slot * C::KV_TILE_BYTES, half, acc);
       };
 
@@ -607,8 +611,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
               acc0 = f2_add(acc0, f2_pack(p0, p1));
               acc1 = f2_add(acc1, f2_pack(p2, p3));
-              pk[c] = pack_bf16x2(p0, p1);
-              pk[c + 1] = pack_bf16x2(p2, p3);
+              pk[c] = F16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+              pk[c + 1] = F16 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
             }
             tmem_st32(t_lane + col_s + 32 * i, pk);
           } else {
@@ -653,7 +657,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       // ---------------------------------------------------------- epilogue
       const size_t lse_idx = (static_cast<size_t>(U.b) * P.Hq + U.hq) * P.Sq + row;
-      __nv_bfloat16* orow =
+      uint16_t* orow =
           P.o + ((static_cast<size_t>(U.b) * P.Sq + row) * P.Hq + U.hq) * static_cast<size_t>(D);
       if (n > 0) {
         bool w = wait_bounded(BAR_O_FULL + 8 * t, oc & 1u, ctl, P);
@@ -671,7 +675,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
-            pk[c] = pack_bf16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv);
+            pk[c] = F16 ? pack_f16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv)
+                        : pack_bf16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv);
           if (row_ok) {
             uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
 #pragma unroll

@@ -43,7 +43,7 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
                          const __grid_constant__ CUtensorMap tm_b, const uint8_t* a_raw,
                          float* out, int* err) {
   constexpr int D = 128;
-  using C = Cfg<D, FP8>;
+  using C = Cfg<D, FP8, false>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

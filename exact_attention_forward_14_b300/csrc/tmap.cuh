@@ -31,14 +31,14 @@ inline bool get_encoder() {
   return encoder_slot() != nullptr;
 }
 
-// Tensor map over a dense [B, S, H, d] tensor (bf16 or 8-bit), dimensions
+// Tensor map over a dense [B, S, H, d] tensor (bf16, fp16 or 8-bit), dimensions
 // listed innermost first as (d, H, S, B) so the byte strides increase. One box
 // is `box_elems` consecutive columns of one head for `box_rows` consecutive
 // rows, landing in shared memory as box_rows rows of box_elems * esz bytes,
 // swizzled in 16-byte units over a 128-byte (or 64-byte) span. Rows past S
 // read as zero. Returns true on success.
 inline bool encode_bshd(CUtensorMap* map, const void* base, bool fp8, int B, int S, int H, int d,
-                        int box_elems, int box_rows) {
+                        int box_elems, int box_rows, bool f16 = false) {
   const uint64_t esz = fp8 ? 1 : 2;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)S, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)(d * esz), (cuuint64_t)((uint64_t)H * d * esz),
@@ -48,7 +48,10 @@ inline bool encode_bshd(CUtensorMap* map, const void* base, bool fp8, int B, int
   const CUtensorMapSwizzle swz =
       box_elems * esz == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
   CUresult r = encoder_slot()(
-      map, fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+      map,
+      fp8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+          : (f16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16),
+      4,
       const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -8,8 +8,9 @@ Recipe (all on the CPU, one ``torch.Generator`` per workload):
   * for the FP8 workload, after each tensor's values a Bernoulli(0.001) mask is
     drawn from the same generator and the selected entries are multiplied by 20
     (outliers);
-  * bf16 workloads round the fp32 draw to bf16 (round-to-nearest-even, torch's
-    cast); the FP8 workload hands the fp32 draw to the block quantiser.
+  * bf16 / fp16 workloads round the fp32 draw to that type (round-to-nearest-
+    even, torch's cast); the FP8 workload hands the fp32 draw to the block
+    quantiser.
 The pages' own benchmark shape is "sequence length 8K, head dim 128"; no public
 dataset is involved.
 """
@@ -32,7 +33,7 @@ class Workload:
     Sk: int
     d: int
     causal: bool
-    dtype: str = "bf16"          # "bf16" or "e4m3"
+    dtype: str = "bf16"          # "bf16", "f16" or "e4m3"
     outlier_frac: float = 0.0
     seed: int = 1000
 
@@ -59,6 +60,9 @@ WORKLOADS = {
                                                 16384, 16384, 128, True, seed=1003),
     "fp8_b4h16s4096d128": Workload("fp8_b4h16s4096d128", 4, 16, 16, 4096, 4096, 128, False,
                                    dtype="e4m3", outlier_frac=0.001, seed=1004),
+    # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
+    "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
+                                          True, dtype="f16", seed=1005),
 }
 
 
@@ -83,6 +87,23 @@ def draw_qkv_bf16(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac=0.0):
     """bf16 CPU tensors (the fp32 draw rounded to bf16)."""
     return tuple(t.to(torch.bfloat16) for t in
                  draw_qkv_f32(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac))
+
+
+def draw_qkv_f16(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac=0.0):
+    """fp16 CPU tensors (the fp32 draw rounded to fp16)."""
+    return tuple(t.to(torch.float16) for t in
+                 draw_qkv_f32(B, Hq, Hkv, Sq, Sk, d, seed, outlier_frac))
+
+
+def draw_workload_16(w: Workload):
+    """The workload's q, k, v in its 16-bit type (bf16 or f16)."""
+    f = draw_qkv_f16 if w.dtype == "f16" else draw_qkv_bf16
+    return f(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
+
+
+def bits16(t: torch.Tensor) -> np.ndarray:
+    """Raw uint16 bits of a bf16 or fp16 CPU tensor, as numpy (for the oracle)."""
+    return t.contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

@@ -19,7 +19,7 @@
  *
  * Layouts (all dense, row-major, no padding):
  *   q, o : [B, Sq, Hq, d]     k, v : [B, Sk, Hkv, d]     lse : [B, Hq, Sq] fp32
- * O is always written as bf16.
+ * O has the inputs' 16-bit type (bf16 or fp16); for E4M3 inputs it is bf16.
  *
  * Ownership and execution: every pointer is a DEVICE pointer owned by the
  * caller. The library allocates no device memory, holds no per-call workspace
@@ -57,8 +57,9 @@ typedef enum {
 } attn_status_t;
 
 typedef enum {
-    ATTN_BF16 = 0,    /* q, k, v are bf16 */
-    ATTN_FP8_E4M3 = 1 /* q, k, v are OCP E4M3 codes with unit scales */
+    ATTN_BF16 = 0,     /* q, k, v and o are bf16 */
+    ATTN_FP8_E4M3 = 1, /* q, k, v are OCP E4M3 codes with unit scales; o is bf16 */
+    ATTN_F16 = 2       /* q, k, v and o are IEEE fp16 (P is kept in fp16 too) */
 } attn_dtype_t;
 
 /* Rows of one FP8 scale block (per batch, head and block of consecutive
@@ -68,7 +69,7 @@ typedef enum {
 /*
  * attn_fwd -- fused attention forward.
  *   q, k, v : device inputs in the layouts above, element type `dtype`
- *   o       : device output, bf16 [B, Sq, Hq, d]
+ *   o       : device output [B, Sq, Hq, d]: fp16 for ATTN_F16, else bf16
  *   lse     : device output, fp32 [B, Hq, Sq]
  *   B, Hq, Hkv, Sq, Sk, d : sizes; Hq % Hkv == 0; d in {64, 128}
  *   causal  : 0 or non-zero (bottom-right causal mask)

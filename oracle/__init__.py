@@ -25,6 +25,7 @@ _lib = None
 
 DTYPE_BF16 = 0
 DTYPE_E4M3 = 1
+DTYPE_F16 = 2
 FP8_BLOCK_ROWS = 64
 
 
@@ -46,6 +47,8 @@ def _load():
         if _lib is not None:
             return _lib
         lib = ctypes.CDLL(build())
+        lib.oracle_f16_decode.restype = ctypes.c_double
+        lib.oracle_f16_decode.argtypes = [ctypes.c_uint16]
         lib.oracle_e4m3_decode.restype = ctypes.c_double
         lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
         lib.oracle_e4m3_encode.restype = ctypes.c_uint8
@@ -69,6 +72,15 @@ def e4m3_decode(codes: np.ndarray) -> np.ndarray:
     lib = _load()
     table = np.array([lib.oracle_e4m3_decode(c) for c in range(256)], dtype=np.float64)
     return table[np.asarray(codes, dtype=np.uint8)]
+
+
+def f16_decode(bits: np.ndarray) -> np.ndarray:
+    """fp64 value of each IEEE binary16 bit pattern (uint16)."""
+    lib = _load()
+    flat = np.asarray(bits, dtype=np.uint16).ravel()
+    out = np.fromiter((lib.oracle_f16_decode(int(b)) for b in flat), dtype=np.float64,
+                      count=flat.size)
+    return out.reshape(np.shape(bits))
 
 
 def e4m3_encode(x: np.ndarray) -> np.ndarray:
@@ -96,8 +108,9 @@ def attn_fwd(q, k, v, causal: bool, scale: float, dtype: str = "bf16",
              q_scale=None, k_scale=None, v_scale=None, rows=None):
     """fp64 exact attention forward.
 
-    q: [B, Sq, Hq, d], k/v: [B, Sk, Hkv, d], given as raw bits: uint16 (bf16)
-    for dtype 'bf16', uint8 E4M3 codes plus fp32 block scales for 'e4m3'.
+    q: [B, Sq, Hq, d], k/v: [B, Sk, Hkv, d], given as raw bits: uint16 for
+    dtype 'bf16' or 'f16' (IEEE half), uint8 E4M3 codes plus fp32 block scales
+    for 'e4m3'.
     Returns (o, lse): o fp64 [B, Sq, Hq, d], lse fp64 [B, Hq, Sq]; or, when
     ``rows`` lists flat indices (b*Hq + hq)*Sq + i, o [n, d] and lse [n].
     """
@@ -106,6 +119,9 @@ def attn_fwd(q, k, v, causal: bool, scale: float, dtype: str = "bf16",
     _, Sk, Hkv, _ = k.shape
     if dtype == "bf16":
         code = DTYPE_BF16
+        want = np.uint16
+    elif dtype == "f16":
+        code = DTYPE_F16
         want = np.uint16
     elif dtype == "e4m3":
         code = DTYPE_E4M3

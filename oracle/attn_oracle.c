@@ -37,6 +37,9 @@
  *   - a row with no visible key has O = 0 and LSE = -inf;
  *   - LSE is the natural logarithm.
  *
+ * FP16 inputs (the page's own benchmark precision, section 6): element value =
+ * the IEEE binary16 value of the bits.
+ *
  * FP8 inputs: element value = decode_e4m3(code) * scale[b, h, row / 64], the
  * block being 64 consecutive sequence rows of one head times all d columns.
  * The quantiser that produces these codes follows [FA3 s4]: per block,
@@ -53,6 +56,7 @@
 
 #define ORACLE_DTYPE_BF16 0
 #define ORACLE_DTYPE_E4M3 1
+#define ORACLE_DTYPE_F16 2
 #define ORACLE_FP8_BLOCK_ROWS 64
 
 /* ---------------------------------------------------------------- codecs -- */
@@ -63,6 +67,19 @@ static double bf16_bits_to_double(uint16_t h) {
     float f;
     memcpy(&f, &u, sizeof f);
     return (double)f;
+}
+
+/* IEEE 754 binary16: 1 sign bit, 5 exponent bits with bias 15, 10 fraction
+ * bits; exponent field 0 encodes subnormals f * 2^-24; field 31 is inf / NaN. */
+double oracle_f16_decode(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int e = (h >> 10) & 0x1F;
+    int f = h & 0x3FF;
+    double mag;
+    if (e == 0x1F) mag = f ? NAN : INFINITY;
+    else if (e == 0) mag = ldexp((double)f, -24);
+    else mag = ldexp(1.0 + (double)f / 1024.0, e - 15);
+    return sign ? -mag : mag;
 }
 
 /* OCP 8-bit floating point, E4M3 ("fn" variant): 1 sign bit, 4 exponent bits
@@ -156,6 +173,7 @@ static double load_elem(const oracle_inputs* in, const void* base, const float* 
                         int S, int H, int b, int s, int h, int c) {
     size_t idx = (((size_t)b * S + s) * H + h) * (size_t)in->d + c;
     if (in->dtype == ORACLE_DTYPE_BF16) return bf16_bits_to_double(((const uint16_t*)base)[idx]);
+    if (in->dtype == ORACLE_DTYPE_F16) return oracle_f16_decode(((const uint16_t*)base)[idx]);
     int nblk = (S + ORACLE_FP8_BLOCK_ROWS - 1) / ORACLE_FP8_BLOCK_ROWS;
     double sc = (double)scale[((size_t)b * H + h) * nblk + s / ORACLE_FP8_BLOCK_ROWS];
     return oracle_e4m3_decode(((const uint8_t*)base)[idx]) * sc;
@@ -221,7 +239,8 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v,
                     int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal, double scale,
                     const int64_t* rows, int64_t nrows) {
     if (check_dims(B, Hq, Hkv, Sq, Sk, d)) return 1;
-    if (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_E4M3) return 1;
+    if (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_E4M3 && dtype != ORACLE_DTYPE_F16)
+        return 1;
     if (dtype == ORACLE_DTYPE_E4M3 && (!q_scale || !k_scale || !v_scale)) return 1;
     oracle_inputs in = {q, k, v, q_scale, k_scale, v_scale, dtype, B, Hq, Hkv, Sq, Sk, d};
     int64_t total = rows ? nrows : (int64_t)B * Hq * Sq;

@@ -20,12 +20,22 @@ def bf16_atol(ref, floor=1e-2):
     return np.maximum(floor, np.exp2(e - 7))
 
 
+def f16_atol(ref, floor=1e-2):
+    """Per-element bound on an fp16 O: max(floor, one fp16 ulp of the reference)."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(ref, 1e-30)))
+    return np.maximum(floor, np.exp2(e - 10))
+
+
 def assert_o_close(o_gpu, o_ref, kind="bf16"):
     o_gpu = np.asarray(o_gpu, dtype=np.float64)
     o_ref = np.asarray(o_ref, dtype=np.float64)
     assert np.isfinite(o_gpu).all(), "non-finite output"
     err = np.abs(o_gpu - o_ref)
-    tol = bf16_atol(o_ref, 1e-2 if kind == "bf16" else 6e-2)
+    if kind == "f16":
+        tol = f16_atol(o_ref)
+    else:
+        tol = bf16_atol(o_ref, 1e-2 if kind == "bf16" else 6e-2)
     bad = err > tol
     assert not bad.any(), (f"{int(bad.sum())} of {bad.size} outside tolerance; "
                            f"max err {err.max():.3e} at {np.unravel_index(err.argmax(), err.shape)}")

@@ -300,3 +300,41 @@ def test_fp8_attention_equals_bf16_attention_on_dequantised_values(oracle_mod):
                                       scales[0][:, :, np.arange(S) // 64].transpose(0, 2, 1)[..., None])
         np.testing.assert_allclose(o8, o16, rtol=0, atol=1e-12)
         np.testing.assert_allclose(l8, l16, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------------ fp16 inputs --
+
+def test_f16_decode_known_values(oracle_mod):
+    """Values fixed by the binary16 definition: 1, the smallest subnormal
+    2^-24, the largest finite 65504, signed zero and infinity."""
+    table = {0x3C00: 1.0, 0x0001: 2.0 ** -24, 0x0400: 2.0 ** -14, 0x7BFF: 65504.0,
+             0xC000: -2.0, 0x8000: -0.0, 0x3555: 1365 / 4096, 0x7C00: np.inf, 0xFC00: -np.inf}
+    got = oracle_mod.f16_decode(np.array(list(table), dtype=np.uint16))
+    np.testing.assert_array_equal(got, np.array(list(table.values())))
+    assert np.isnan(oracle_mod.f16_decode(np.array([0x7E00, 0xFC01], dtype=np.uint16))).all()
+
+
+def test_f16_decode_matches_torch_on_every_pattern(oracle_mod):
+    bits = np.arange(0, 1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = torch.from_numpy(bits.view(np.int16)).view(torch.float16).to(torch.float64).numpy()
+    got = oracle_mod.f16_decode(bits)
+    nan = np.isnan(ref)
+    np.testing.assert_array_equal(np.isnan(got), nan)
+    np.testing.assert_array_equal(got[~nan], ref[~nan])
+
+
+def test_f16_attention_equals_bf16_attention_on_shared_values(oracle_mod):
+    """Multiples of 1/16 up to +-7.9375 are exact in both bf16 and fp16, so the
+    two 16-bit input paths must give identical results on them."""
+    rng = np.random.default_rng(17)
+    B, Hq, Hkv, S, d = 2, 4, 2, 37, 8
+    vals = [rng.integers(-127, 128, size=(B, S, h, d)) / 16.0 for h in (Hq, Hkv, Hkv)]
+    as_f16 = [torch.tensor(v, dtype=torch.float16).view(torch.int16).numpy().view(np.uint16)
+              for v in vals]
+    as_bf16 = [torch.tensor(v, dtype=torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+               for v in vals]
+    for causal in (False, True):
+        o_h, l_h = oracle_mod.attn_fwd(*as_f16, causal, 0.3, dtype="f16")
+        o_b, l_b = oracle_mod.attn_fwd(*as_bf16, causal, 0.3, dtype="bf16")
+        np.testing.assert_array_equal(o_h, o_b)
+        np.testing.assert_array_equal(l_h, l_b)

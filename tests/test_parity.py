@@ -122,3 +122,48 @@ def test_tiny_workload_full(oracle_mod):
 ])
 def test_full_size_workloads_sampled_rows(oracle_mod, name, n_rows):
     _full_size_rows(oracle_mod, inputs.WORKLOADS[name], n_rows)
+
+
+# ------------------------------------------------------------ fp16 inputs --
+# (B, Hq, Hkv, Sq, Sk, d, causal): d = 64 and 128, GQA, ragged tails, Sq != Sk
+SMALL_F16 = [
+    (1, 2, 2, 128, 128, 128, False),
+    (2, 4, 2, 300, 300, 128, True),
+    (1, 2, 2, 127, 300, 64, True),
+    (1, 4, 1, 600, 513, 128, False),
+    (1, 2, 2, 300, 127, 128, True),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", SMALL_F16, ids=lambda s: "f16_b{}hq{}hkv{}sq{}sk{}d{}{}".format(
+    *s[:6], "c" if s[6] else ""))
+def test_f16_small_full_compare(oracle_mod, shape):
+    torch = require_gpu()
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = inputs.draw_qkv_f16(B, Hq, Hkv, Sq, Sk, d, seed=sum(shape) + 29)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=causal, scale=scale)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    assert o.dtype == torch.float16
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
+                                         causal, scale, dtype="f16")
+    assert_o_close(o.float().cpu().numpy(), o_ref, kind="f16")
+    assert_lse_close(lse.cpu().numpy(), lse_ref)
+
+
+@pytest.mark.gpu
+def test_f16_full_size_sampled_rows(oracle_mod):
+    torch = require_gpu()
+    w = inputs.WORKLOADS["f16_b2h32s8192d128_causal"]
+    q, k, v = inputs.draw_workload_16(w)
+    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rows = inputs.sample_rows(w.B, w.Hq, w.Sq, 1200, seed=w.seed)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
+                                         w.causal, w.scale, dtype="f16", rows=rows)
+    b, rem = np.divmod(rows, w.Hq * w.Sq)
+    h, i = np.divmod(rem, w.Sq)
+    o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
+    assert_o_close(o_g, o_ref, kind="f16")
+    assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref)
