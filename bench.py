@@ -244,10 +244,13 @@ def run_reference(args, w):
     return 0
 
 
-def workload_config(w):
-    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
-            "d": w.d, "causal": w.causal, "dtype": w.dtype,
-            "l2": "inputs larger than L2 (no flush)"}
+def workload_config(w, nsplit=None):
+    c = {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "Sq": w.Sq, "Sk": w.Sk,
+         "d": w.d, "causal": w.causal, "dtype": w.dtype,
+         "l2": "inputs larger than L2 (no flush)"}
+    if nsplit:
+        c["splitkv_ranges"] = nsplit
+    return c
 
 
 # ------------------------------------------------------ rank arithmetic --
@@ -304,8 +307,25 @@ def run_ours(args, w):
     lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    ws, nsplit = None, 0
+    if w.splits:
+        nsplit = w.splits
+        rc, planned, wbytes = ea.attn_splitkv_plan(w.B, w.Hq, w.Sq, w.Sk, w.d, w.causal)
+        if rc != ea.ATTN_OK:
+            raise ea.AttnError(rc, "attn_splitkv_plan")
+        if nsplit < 0:
+            nsplit = planned
+        wbytes = nsplit * w.B * w.Hq * w.Sq * (w.d + 1) * 4
+        ws = torch.empty(wbytes // 4, dtype=torch.float32, device=dev)
+
     def step():
-        if w.dtype == "e4m3":
+        if ws is not None:
+            q, k, v = dev_in
+            rc = ea.attn_fwd_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
+                                     w.causal, w.scale,
+                                     ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, nsplit,
+                                     ws, ws.numel() * 4, stream)
+        elif w.dtype == "e4m3":
             q8, k8, v8, qs, ks, vs = dev_in
             rc = ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk,
                                  w.d, w.causal, w.scale, stream)
@@ -408,8 +428,8 @@ def run_ours(args, w):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
-        "config": workload_config(w), "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": args.steps, "roofline": roofline,
+        "config": workload_config(w, nsplit), "clocks": clocks.summary(), "e2e": e2e,
+        "gpu_launches": args.steps * (2 if ws is not None else 1), "roofline": roofline,
     }
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)

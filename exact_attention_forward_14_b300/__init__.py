@@ -19,8 +19,10 @@ import threading
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
     "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "ATTN_F16", "AttnError",
-    "attn_fwd", "attn_fwd_fp8", "attn_quantize_fp8_e4m3", "attn_device_status",
-    "attn_status_string", "forward", "forward_fp8", "quantize_fp8", "library_path", "load",
+    "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_splitkv_plan",
+    "attn_quantize_fp8_e4m3", "attn_device_status",
+    "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
+    "library_path", "load",
 ]
 
 ATTN_OK = 0
@@ -67,6 +69,12 @@ def load():
         lib.attn_fwd.restype = I
         lib.attn_fwd_fp8.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, P]
         lib.attn_fwd_fp8.restype = I
+        lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P,
+                                         ctypes.c_size_t, P]
+        lib.attn_fwd_splitkv.restype = I
+        lib.attn_splitkv_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
+                                          ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_splitkv_plan.restype = I
         lib.attn_quantize_fp8_e4m3.argtypes = [P, P, P, I, I, I, I, P]
         lib.attn_quantize_fp8_e4m3.restype = I
         lib.attn_device_status.argtypes = [P]
@@ -110,6 +118,23 @@ def attn_fwd_fp8(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk,
                                _ptr(v_scale), _ptr(o), _ptr(lse), int(B), int(Hq), int(Hkv),
                                int(Sq), int(Sk), int(d), int(bool(causal)), float(scale),
                                _stream(stream))
+
+
+def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype, num_splits,
+                     workspace, workspace_bytes, stream=None) -> int:
+    return load().attn_fwd_splitkv(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                   int(Hq), int(Hkv), int(Sq), int(Sk), int(d),
+                                   int(bool(causal)), float(scale), int(dtype), int(num_splits),
+                                   _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_splitkv_plan(B, Hq, Sq, Sk, d, causal=False, num_sms=0):
+    """Returns (status, num_splits, workspace_bytes)."""
+    n = ctypes.c_int(0)
+    w = ctypes.c_size_t(0)
+    rc = load().attn_splitkv_plan(int(B), int(Hq), int(Sq), int(Sk), int(d), int(bool(causal)),
+                                  int(num_sms), ctypes.byref(n), ctypes.byref(w))
+    return rc, n.value, w.value
 
 
 def attn_quantize_fp8_e4m3(x, codes, scale, B, S, H, d, stream=None) -> int:
@@ -176,6 +201,33 @@ def forward_fp8(q, k, v, q_scale, k_scale, v_scale, causal: bool = False,
         lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
     _check(attn_fwd_fp8(q, k, v, q_scale, k_scale, v_scale, out, lse, B, Hq, Hkv, Sq, Sk, d,
                         causal, scale, stream), "attn_fwd_fp8")
+    return out, lse
+
+
+def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
+                    num_splits: int | None = None, workspace=None, out=None, lse=None,
+                    stream=None):
+    """Split-KV forward (bf16 or fp16). num_splits None = attn_splitkv_plan's
+    choice; the fp32 workspace is allocated with torch unless given."""
+    import torch
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    code = ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if num_splits is None:
+        rc, num_splits, _ = attn_splitkv_plan(B, Hq, Sq, Sk, d, causal)
+        _check(rc, "attn_splitkv_plan")
+    need = num_splits * B * Hq * Sq * (d + 1) * 4
+    if workspace is None:
+        workspace = torch.empty(need // 4, dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Sq, Hq, d), dtype=q.dtype, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    _check(attn_fwd_splitkv(q, k, v, out, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, code,
+                            num_splits, workspace, workspace.numel() * workspace.element_size(),
+                            stream), "attn_fwd_splitkv")
     return out, lse
 
 

@@ -16,6 +16,7 @@
 #include "attn_b300.h"
 #include "attn_fwd_kernel.cuh"
 #include "quantize_fp8.cuh"
+#include "splitkv_combine.cuh"
 #include "tmap.cuh"
 
 namespace {
@@ -30,6 +31,7 @@ __device__ int g_attn_status = 0;
 
 constexpr int kMaxDevices = 64;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr int kMaxSplits = 256;  // key ranges per split-KV call
 
 struct DeviceInfo {
   std::once_flag once;
@@ -84,10 +86,21 @@ bool fits_i32(long long a, long long b, long long c, long long d) {
   return x <= lim;
 }
 
+// Key-range split of one launch: nsplit ranges of kps K/V tiles each (kps = 0:
+// all tiles); partial outputs go to o_part / lse_part when those are set.
+struct Split {
+  int nsplit;
+  int kps;
+  float* o_part;
+  float* lse_part;
+};
+constexpr Split kNoSplit = {1, 0, nullptr, nullptr};
+
 template <int D, bool FP8, bool F16>
 int launch(const void* q, const void* k, const void* v, const float* qs, const float* ks,
            const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk,
-           int causal, float scale, cudaStream_t stream, DeviceInfo* di, uint32_t attr_bit) {
+           int causal, float scale, cudaStream_t stream, DeviceInfo* di, uint32_t attr_bit,
+           const Split& sp) {
   using C = Cfg<D, FP8, F16>;
   auto kern = attnb3::attn_fwd_kernel<D, FP8, F16>;
   if (!(di->attr_done.load(std::memory_order_acquire) & attr_bit)) {
@@ -117,7 +130,11 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
   P.n_qp = (Sq + attnb3::UNIT_ROWS - 1) / attnb3::UNIT_ROWS;
   P.npair = (P.n_qp + 1) / 2;
   P.nkv = (Sk + attnb3::BN - 1) / attnb3::BN;
-  P.num_items = B * Hq * P.npair;
+  P.nsplit = sp.nsplit;
+  P.kps = sp.kps > 0 ? sp.kps : P.nkv;
+  P.o_part = sp.o_part;
+  P.lse_part = sp.lse_part;
+  P.num_items = B * Hq * P.npair * P.nsplit;
   P.causal = causal ? 1 : 0;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.timeout_ns = kWaitLimitNs;
@@ -144,30 +161,58 @@ int check_attn_args(const void* q, const void* k, const void* v, void* o, float*
 
 int run_attn(const void* q, const void* k, const void* v, const float* qs, const float* ks,
              const float* vs, void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
-             int causal, float scale, bool fp8, bool f16, cudaStream_t stream) {
+             int causal, float scale, bool fp8, bool f16, cudaStream_t stream,
+             const Split& sp = kNoSplit) {
   DeviceInfo* di = nullptr;
   int rc = current_device(&di);
   if (rc != ATTN_OK) return rc;
   if (!get_encoder()) return ATTN_ERR_CUDA;
   if (fp8 && d == 128)
     return launch<128, true, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                    scale, stream, di, 4u);
+                                    scale, stream, di, 4u, sp);
   if (fp8 && d == 64)
     return launch<64, true, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                   scale, stream, di, 8u);
+                                   scale, stream, di, 8u, sp);
   if (f16 && d == 128)
     return launch<128, false, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                    scale, stream, di, 16u);
+                                    scale, stream, di, 16u, sp);
   if (f16 && d == 64)
     return launch<64, false, true>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                   scale, stream, di, 32u);
+                                   scale, stream, di, 32u, sp);
   if (d == 128)
     return launch<128, false, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                     scale, stream, di, 1u);
+                                     scale, stream, di, 1u, sp);
   if (d == 64)
     return launch<64, false, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
-                                    scale, stream, di, 2u);
+                                    scale, stream, di, 2u, sp);
   return ATTN_ERR_UNSUPPORTED;
+}
+
+// K/V tiles per range and the number of non-empty ranges for a requested
+// split count.
+void split_shape(int Sk, int num_splits, int* kps, int* nsplit) {
+  const int nkv = (Sk + attnb3::BN - 1) / attnb3::BN;
+  const int want = num_splits < nkv ? num_splits : nkv;
+  *kps = (nkv + want - 1) / want;
+  *nsplit = (nkv + *kps - 1) / *kps;
+}
+
+size_t splitkv_bytes(int B, int Hq, int Sq, int d, int nsplit) {
+  const size_t rows = static_cast<size_t>(B) * Hq * Sq;
+  return static_cast<size_t>(nsplit) * rows * static_cast<size_t>(d + 1) * sizeof(float);
+}
+
+template <int D, bool F16>
+int launch_combine(const float* o_part, const float* lse_part, void* o, float* lse, int B, int Hq,
+                   int Sq, int nsplit, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * Hq * Sq;
+  const long long per_block = attnb3::COMBINE_THREADS / 32;
+  const long long blocks = (rows + per_block - 1) / per_block;
+  if (blocks > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  attnb3::splitkv_combine_kernel<D, F16>
+      <<<static_cast<unsigned>(blocks), attnb3::COMBINE_THREADS, 0, stream>>>(
+          o_part, lse_part, static_cast<uint16_t*>(o), lse, B, Hq, Sq, nsplit);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 }  // namespace
@@ -198,6 +243,75 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_sca
     return ATTN_ERR_MISALIGNED;
   return run_attn(q, k, v, q_scale, k_scale, v_scale, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
                   scale, true, false, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int attn_splitkv_plan(int B, int Hq, int Sq, int Sk, int d, int causal, int num_sms,
+                      int* num_splits, size_t* workspace_bytes) {
+  if (!num_splits || !workspace_bytes) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Hq <= 0 || Sq <= 0 || Sk <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (num_sms <= 0) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return ATTN_ERR_CUDA;
+  }
+  // Cost model (uniform units): a launch takes ceil(items * s / num_sms) rounds
+  // of work items, each ceil(tiles / s) K/V tiles plus ~2 tiles of per-range
+  // overhead (pipeline fill, partial write, merge). Under a causal mask a unit
+  // sees on average the key tiles minus half the query tiles.
+  const long long nkv = (Sk + attnb3::BN - 1) / attnb3::BN;
+  const long long nqt = (Sq + attnb3::BM - 1) / attnb3::BM;
+  const long long n_qp = (Sq + attnb3::UNIT_ROWS - 1) / attnb3::UNIT_ROWS;
+  const long long items = static_cast<long long>(B) * Hq * ((n_qp + 1) / 2);
+  long long tiles = causal ? nkv - nqt / 2 : nkv;
+  if (tiles < 1) tiles = 1;
+  long long smax = nkv / 4 > 1 ? nkv / 4 : 1;  // >= 4 K/V tiles per range
+  if (smax > kMaxSplits) smax = kMaxSplits;
+  long long best = 1, best_cost = -1;
+  for (long long s = 1; s <= smax; ++s) {
+    const long long rounds = (items * s + num_sms - 1) / num_sms;
+    const long long cost = rounds * ((tiles + s - 1) / s + 2);
+    if (best_cost < 0 || cost < best_cost) {
+      best = s;
+      best_cost = cost;
+    }
+  }
+  int kps = 0, nsplit = 0;
+  split_shape(Sk, static_cast<int>(best), &kps, &nsplit);
+  *num_splits = nsplit;
+  *workspace_bytes = splitkv_bytes(B, Hq, Sq, d, nsplit);
+  return ATTN_OK;
+}
+
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse, int B,
+                     int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale, int dtype,
+                     int num_splits, void* workspace, size_t workspace_bytes,
+                     attn_stream_t stream) {
+  int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  int kps = 0, nsplit = 0;
+  split_shape(Sk, num_splits, &kps, &nsplit);
+  const size_t need = splitkv_bytes(B, Hq, Sq, d, nsplit);
+  if (!workspace || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(workspace, 16)) return ATTN_ERR_MISALIGNED;
+  const long long n_qp = (Sq + attnb3::UNIT_ROWS - 1) / attnb3::UNIT_ROWS;
+  if (static_cast<long long>(B) * Hq * ((n_qp + 1) / 2) * nsplit > 0x7fffffffLL)
+    return ATTN_ERR_INVALID_ARG;
+  float* o_part = static_cast<float*>(workspace);
+  float* lse_part = o_part + static_cast<size_t>(nsplit) * B * Hq * Sq * d;
+  const bool f16 = dtype == ATTN_F16;
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  rc = run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale,
+                false, f16, st, Split{nsplit, kps, o_part, lse_part});
+  if (rc != ATTN_OK) return rc;
+  if (d == 128)
+    return f16 ? launch_combine<128, true>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st)
+               : launch_combine<128, false>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st);
+  return f16 ? launch_combine<64, true>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st)
+             : launch_combine<64, false>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st);
 }
 
 int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, int S, int H,

@@ -80,8 +80,16 @@ struct FwdParams {
   int n_qp;       // ceil(Sq / UNIT_ROWS): units (levels) per (b, hq)
   int npair;      // ceil(n_qp / 2): work items per (b, hq)
   int nkv;        // ceil(Sk / BN)
-  int num_items;  // B * Hq * npair
+  int num_items;  // B * Hq * npair * nsplit
   int causal;
+  // Split-KV (nsplit > 1, or o_part set): the K/V tiles are cut into ranges
+  // of kps tiles; a work item covers one range and its epilogue writes the
+  // range's normalised O (fp32) and LSE to o_part / lse_part instead of o /
+  // lse. nsplit = 1, kps = nkv, o_part = null is the plain forward pass.
+  int nsplit;
+  int kps;
+  float* o_part;    // [nsplit, B, Hq, Sq, d] fp32
+  float* lse_part;  // [nsplit, B, Hq, Sq] fp32
   float scale_log2;  // softmax scale * log2(e)
   unsigned long long timeout_ns;
   int* status;       // device status word
@@ -192,6 +200,7 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
 
 struct Unit {
   int b, hq, hkv, row0;
+  int split, j0;  // key range: K/V tiles j0 + [0, n[t])
   int n[2];  // K/V tiles needed by Q tile 0 / 1 (0 = tile idle or fully masked)
   int nmax;
 };
@@ -206,8 +215,13 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // Items are numbered (b, hq)-major with hq fastest: the CTAs running at the
 // same time cover only a few heads (query heads sharing a KV head are
 // adjacent), so those heads' K/V tiles are re-read from L2, not HBM.
+// With split-KV, item w covers key range w % nsplit of pair w / nsplit.
 // Returns false when item w has no k-th unit (odd n_qp, middle level).
 __device__ __forceinline__ bool decode_unit(int w, int k, const FwdParams& P, Unit& U) {
+  U.split = w % P.nsplit;
+  w /= P.nsplit;
+  U.j0 = U.split * P.kps;
+  const int j1 = min(U.j0 + P.kps, P.nkv);
   const int bh = w / P.npair;
   const int p = w - bh * P.npair;
   const int level = k == 0 ? P.n_qp - 1 - p : p;
@@ -229,7 +243,7 @@ __device__ __forceinline__ bool decode_unit(int w, int k, const FwdParams& P, Un
         n = lim <= 0 ? 0 : min(ceil_div(lim, BN), P.nkv);
       }
     }
-    U.n[t] = n;
+    U.n[t] = max(0, min(n, j1) - U.j0);
   }
   U.nmax = max(U.n[0], U.n[1]);
   return true;
@@ -368,7 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             for (int c = 0; c < C::NCHUNK; ++c)
               tma_load_4d(sbase + C::OFF_KV + slot * C::KV_TILE_BYTES + c * C::KV_CHUNK_BYTES,
                           kv ? &tm_v : &tm_k, BAR_KV_FULL + 8 * slot, c * C::CHUNK_ELEMS, U.hkv,
-                          j * BN, U.b);
+                          (U.j0 + j) * BN, U.b);
             ++it;
           }
         }
@@ -531,8 +545,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         // mask: keys past Sk, and (causal) keys after row + Sk - Sq
-        int vis = P.Sk - j * BN;
-        if (P.causal) vis = min(vis, row + (P.Sk - P.Sq) - j * BN + 1);
+        const int key0 = (U.j0 + j) * BN;
+        int vis = P.Sk - key0;
+        if (P.causal) vis = min(vis, row + (P.Sk - P.Sq) - key0 + 1);
         if (vis < BN) {
 #pragma unroll
           for (int c = 0; c < BN; ++c)
@@ -546,7 +561,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         float e_lo = P_SCALE_LOG2, e_hi = P_SCALE_LOG2;
         float inv_lo = 1.f / (1 << static_cast<int>(P_SCALE_LOG2)), inv_hi = inv_lo;
         if (FP8 && ks_row != nullptr) {
-          const int kb0 = 2 * j, kb1 = 2 * j + 1;
+          const int kb0 = 2 * (U.j0 + j), kb1 = kb0 + 1;
           const float vs0 = vs_row[kb0];
           const float vs1 = kb1 < nblk_k ? vs_row[kb1] : v_ref;
           c_lo = cq * ks_row[kb0];
@@ -657,6 +672,40 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       // ---------------------------------------------------------- epilogue
       const size_t lse_idx = (static_cast<size_t>(U.b) * P.Hq + U.hq) * P.Sq + row;
+      if (P.o_part != nullptr) {
+        // split-KV: this key range's O / l (fp32) and LSE, for the combine
+        const size_t pidx =
+            static_cast<size_t>(U.split) * P.B * P.Hq * P.Sq + lse_idx;
+        float* prow = P.o_part + pidx * D;
+        float inv = 0.f;
+        if (n > 0) {
+          bool w = wait_bounded(BAR_O_FULL + 8 * t, oc & 1u, ctl, P);
+          ++oc;
+          if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+          tc_fence_after();
+          inv = l_run > 0.f ? v_ref / (FP8 ? l_run * (1 << static_cast<int>(P_SCALE_LOG2)) : l_run)
+                            : 0.f;
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint32_t r[32];
+            tmem_ld32(t_lane + col_o + 32 * i, r);
+            if (row_ok) {
+              float4* dst = reinterpret_cast<float4*>(prow + 32 * i);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
+                                     __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
+            }
+          }
+        } else if (row_ok) {
+          float4* dst = reinterpret_cast<float4*>(prow);
+#pragma unroll
+          for (int v = 0; v < D / 4; ++v) dst[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (row_ok)
+          P.lse_part[pidx] = (n > 0 && l_run > 0.f) ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
+        continue;
+      }
       uint16_t* orow =
           P.o + ((static_cast<size_t>(U.b) * P.Sq + row) * P.Hq + U.hq) * static_cast<size_t>(D);
       if (n > 0) {

@@ -36,6 +36,7 @@ class Workload:
     dtype: str = "bf16"          # "bf16", "f16" or "e4m3"
     outlier_frac: float = 0.0
     seed: int = 1000
+    splits: int = 0              # split-KV ranges: 0 = plain forward, -1 = the plan's choice
 
     @property
     def scale(self) -> float:
@@ -60,6 +61,13 @@ WORKLOADS = {
                                                 16384, 16384, 128, True, seed=1003),
     "fp8_b4h16s4096d128": Workload("fp8_b4h16s4096d128", 4, 16, 16, 4096, 4096, 128, False,
                                    dtype="e4m3", outlier_frac=0.001, seed=1004),
+    # long key side, short query side (the last 256 rows of a 64K context, GQA):
+    # 32 work items alone leave most SMs idle; the split-KV form fills them
+    "longkv_b1hq32hkv8sq256sk65536d128": Workload("longkv_b1hq32hkv8sq256sk65536d128", 1, 32, 8,
+                                                  256, 65536, 128, False, seed=1006),
+    "longkv_b1hq32hkv8sq256sk65536d128_splitkv": Workload(
+        "longkv_b1hq32hkv8sq256sk65536d128_splitkv", 1, 32, 8, 256, 65536, 128, False,
+        seed=1006, splits=-1),
     # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
     "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
                                           True, dtype="f16", seed=1005),

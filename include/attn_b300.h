@@ -35,6 +35,7 @@
 #ifndef ATTN_B300_H
 #define ATTN_B300_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -99,6 +100,47 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v,
                  const float* q_scale, const float* k_scale, const float* v_scale,
                  void* o, float* lse, int B, int Hq, int Hkv, int Sq, int Sk, int d,
                  int causal, float scale, attn_stream_t stream);
+
+/*
+ * attn_splitkv_plan -- split count and workspace size for attn_fwd_splitkv.
+ * Chooses the number of key ranges s (1..256, at least 4 K/V tiles of 128
+ * keys per range) that minimises a simple cost model: rounds of work items,
+ * ceil(items * s / num_sms), times the K/V tiles per range plus two tiles of
+ * per-range overhead. 1 when the query side alone already fills the GPU in
+ * whole rounds.
+ *   causal          : as attn_fwd (a causal unit sees about half the tiles)
+ *   num_sms         : SMs to fill; <= 0 queries the current device
+ *   num_splits      : out, number of key ranges (>= 1)
+ *   workspace_bytes : out, bytes of device workspace attn_fwd_splitkv needs
+ *                     for that split count
+ * Pure arithmetic unless num_sms <= 0. Returns an attn_status_t.
+ */
+int attn_splitkv_plan(int B, int Hq, int Sq, int Sk, int d, int causal, int num_sms,
+                      int* num_splits, size_t* workspace_bytes);
+
+/*
+ * attn_fwd_splitkv -- the same forward pass with the keys cut into ranges
+ * processed by separate work items, merged by a second kernel (the online-
+ * softmax rescaling of the FlashAttention-3 deep dive, sections 2-3, applied
+ * across key ranges: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s).
+ * Arguments as attn_fwd (dtype ATTN_BF16 or ATTN_F16), plus:
+ *   num_splits      : requested ranges, 1..256 (ranges of ceil(Sk/128/n) K/V
+ *                     tiles; fewer if some would be empty)
+ *   workspace       : device buffer owned by the caller, 16-byte aligned, at
+ *                     least num_splits * B * Hq * Sq * (d + 1) * 4 bytes (what
+ *                     attn_splitkv_plan reports); holds the per-range O (fp32)
+ *                     and LSE between the two kernels; contents on entry are
+ *                     ignored, on return undefined
+ *   workspace_bytes : its size
+ * Two kernels are enqueued on `stream`; calls that share a workspace must not
+ * overlap. Errors: as attn_fwd; ATTN_ERR_INVALID_ARG for a bad split count or a
+ * missing / too small workspace, ATTN_ERR_MISALIGNED for a misaligned one,
+ * ATTN_ERR_UNSUPPORTED for ATTN_FP8_E4M3.
+ */
+int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float* lse,
+                     int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal, float scale,
+                     int dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                     attn_stream_t stream);
 
 /*
  * attn_quantize_fp8_e4m3 -- block quantiser producing attn_fwd_fp8 inputs

@@ -124,3 +124,61 @@ def test_product_package_never_touches_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert not re.search(r"^\s*(import|from)\s+oracle\b", text, flags=re.M), f
                 assert "attn_oracle" not in text and "liboracle" not in text, f
+
+
+# ------------------------------------------------------------------ split-KV --
+
+def _plan_by_hand(B, Hq, Sq, Sk, causal, sms):
+    """The documented cost model, restated: argmin over s of
+    ceil(items * s / sms) * (ceil(tiles / s) + 2), smallest s on ties."""
+    nkv, nqt, nqp = -(-Sk // 128), -(-Sq // 128), -(-Sq // 256)
+    items = B * Hq * ((nqp + 1) // 2)
+    tiles = max(1, nkv - nqt // 2) if causal else nkv
+    smax = min(max(1, nkv // 4), 256)
+    costs = [(-(-items * s // sms) * (-(-tiles // s) + 2), s) for s in range(1, smax + 1)]
+    s = min(costs)[1]
+    kps = -(-nkv // min(s, nkv))
+    return -(-nkv // kps)
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 32, 256, 65536, False),   # 32 items: 9 ranges make two full rounds
+    (1, 8, 64, 65536, False),
+    (2, 32, 8192, 8192, True),    # the query side fills the GPU
+    (4, 16, 2048, 2048, True),
+    (1, 1, 1, 1024, False),
+    (1, 4, 300, 3000, True),
+])
+def test_splitkv_plan_follows_the_cost_model(shape):
+    B, Hq, Sq, Sk, causal = shape
+    rc, n, w = ea.attn_splitkv_plan(B, Hq, Sq, Sk, 128, causal, num_sms=148)
+    assert rc == ea.ATTN_OK
+    assert n == _plan_by_hand(B, Hq, Sq, Sk, causal, 148)
+    assert w == n * B * Hq * Sq * 129 * 4
+
+
+def test_splitkv_plan_examples_and_errors():
+    assert ea.attn_splitkv_plan(1, 32, 256, 65536, 128, False, num_sms=148)[1] == 9
+    assert ea.attn_splitkv_plan(2, 32, 8192, 8192, 128, True, num_sms=148)[1] == 1
+    assert ea.attn_splitkv_plan(1, 1, 1, 100, 96, False, num_sms=148)[0] == ea.ATTN_ERR_UNSUPPORTED
+    assert ea.attn_splitkv_plan(0, 1, 1, 100, 64, False, num_sms=148)[0] == ea.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(num_splits=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(num_splits=257), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=16), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=0x60008), ea.ATTN_ERR_MISALIGNED),
+    (dict(dtype=ea.ATTN_FP8_E4M3), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(Hkv=3), ea.ATTN_ERR_INVALID_ARG),
+])
+def test_splitkv_rejects_bad_arguments(lib, kw, code):
+    a = dict(B=1, Hq=4, Hkv=2, Sq=64, Sk=1000, d=128, causal=0, scale=0.1, dtype=ea.ATTN_BF16,
+             num_splits=4, workspace=0x60000, workspace_bytes=1 << 30)
+    a.update(kw)
+    rc = ea.attn_fwd_splitkv(Q, K, V, O, L, a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["d"],
+                             a["causal"], a["scale"], a["dtype"], a["num_splits"], a["workspace"],
+                             a["workspace_bytes"], stream=0)
+    assert rc == code

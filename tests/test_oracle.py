@@ -338,3 +338,26 @@ def test_f16_attention_equals_bf16_attention_on_shared_values(oracle_mod):
         o_b, l_b = oracle_mod.attn_fwd(*as_bf16, causal, 0.3, dtype="bf16")
         np.testing.assert_array_equal(o_h, o_b)
         np.testing.assert_array_equal(l_h, l_b)
+
+
+# ------------------------------------------------- merge across key ranges --
+
+def test_merging_key_ranges_reproduces_the_whole(oracle_mod):
+    """The split-KV combine formula, checked on the oracle itself: attention
+    over keys [0, c) and [c, Sk) separately, merged with
+    LSE = ln(e^LSE1 + e^LSE2), O = e^(LSE1 - LSE) O1 + e^(LSE2 - LSE) O2,
+    equals attention over all keys (non-causal; the causal mask is a per-row
+    key range, covered by the GPU tests against the unsplit oracle)."""
+    rng = np.random.default_rng(23)
+    B, Hq, Hkv, Sq, Sk, d = 1, 4, 2, 9, 40, 8
+    q, k, v = (bf16(rng.standard_normal(s) * 2)[0] for s in
+               ((B, Sq, Hq, d), (B, Sk, Hkv, d), (B, Sk, Hkv, d)))
+    o, lse = oracle_mod.attn_fwd(q, k, v, False, 0.4)
+    for c in (1, 13, 39):
+        o1, l1 = oracle_mod.attn_fwd(q, k[:, :c], v[:, :c], False, 0.4)
+        o2, l2 = oracle_mod.attn_fwd(q, k[:, c:], v[:, c:], False, 0.4)
+        lm = np.logaddexp(l1, l2)
+        w1 = np.exp(l1 - lm).transpose(0, 2, 1)[..., None]
+        w2 = np.exp(l2 - lm).transpose(0, 2, 1)[..., None]
+        np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(w1 * o1 + w2 * o2, o, rtol=0, atol=1e-12)
