@@ -19,7 +19,8 @@ import threading
 __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
     "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "ATTN_F16", "AttnError",
-    "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_splitkv_plan",
+    "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc",
+    "attn_splitkv_plan",
     "attn_quantize_fp8_e4m3", "attn_device_status",
     "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
     "library_path", "load",
@@ -72,6 +73,8 @@ def load():
         lib.attn_fwd_splitkv.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P,
                                          ctypes.c_size_t, P]
         lib.attn_fwd_splitkv.restype = I
+        lib.attn_fwd_splitkv_noalloc.argtypes = [P, P, P, P, P, I, I, I, I, I, I, I, F, I, I, P]
+        lib.attn_fwd_splitkv_noalloc.restype = I
         lib.attn_splitkv_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
                                           ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_splitkv_plan.restype = I
@@ -126,6 +129,16 @@ def attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtyp
                                    int(Hq), int(Hkv), int(Sq), int(Sk), int(d),
                                    int(bool(causal)), float(scale), int(dtype), int(num_splits),
                                    _ptr(workspace), int(workspace_bytes), _stream(stream))
+
+
+def attn_fwd_splitkv_noalloc(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype,
+                             num_splits, stream=None) -> int:
+    """attn_fwd_splitkv with the library's built-in 64 MiB workspace (no
+    allocation anywhere; for callers that may not allocate device memory)."""
+    return load().attn_fwd_splitkv_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), int(B),
+                                           int(Hq), int(Hkv), int(Sq), int(Sk), int(d),
+                                           int(bool(causal)), float(scale), int(dtype),
+                                           int(num_splits), _stream(stream))
 
 
 def attn_splitkv_plan(B, Hq, Sq, Sk, d, causal=False, num_sms=0):

@@ -215,6 +215,34 @@ int launch_combine(const float* o_part, const float* lse_part, void* o, float* l
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// ---- workspace for attn_fwd_splitkv_noalloc --------------------------------
+// A fixed device array in this library, so that callers who may not allocate
+// device memory can still use the split-KV path. Every GPU that loads the
+// library holds these bytes until the process exits.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(64) << 20;  // 64 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// The array's device address, looked up once per device (with that device
+// current); in host code the array's name is only a stand-in for it.
+std::once_flag g_scratch_once[kMaxDevices];
+void* g_scratch_ptr[kMaxDevices];
+int g_scratch_rc[kMaxDevices];
+
+int noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
+  std::call_once(g_scratch_once[dev], [dev] {
+    void* ptr = nullptr;
+    g_scratch_rc[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess
+                            ? ATTN_OK
+                            : ATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = ptr;
+  });
+  if (g_scratch_rc[dev] != ATTN_OK) return g_scratch_rc[dev];
+  *out = g_scratch_ptr[dev];
+  return ATTN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -312,6 +340,22 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                : launch_combine<128, false>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st);
   return f16 ? launch_combine<64, true>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st)
              : launch_combine<64, false>(o_part, lse_part, o, lse, B, Hq, Sq, nsplit, st);
+}
+
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal,
+                             float scale, int dtype, int num_splits, attn_stream_t stream) {
+  int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
+  int kps = 0, nsplit = 0;
+  split_shape(Sk, num_splits, &kps, &nsplit);
+  if (splitkv_bytes(B, Hq, Sq, d, nsplit) > kNoAllocScratchBytes) return ATTN_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  rc = noalloc_scratch(&scratch);
+  if (rc != ATTN_OK) return rc;
+  return attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype,
+                          num_splits, scratch, kNoAllocScratchBytes, stream);
 }
 
 int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, int S, int H,

@@ -143,6 +143,32 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
                      attn_stream_t stream);
 
 /*
+ * attn_fwd_splitkv_noalloc -- attn_fwd_splitkv for callers that may not
+ * allocate device memory themselves: for example a plugin inside a host
+ * application that owns every device buffer, or a latency-critical loop that
+ * must not call cudaMalloc / cudaFree (which can synchronise the device) or
+ * that runs under a fixed device-memory budget. It takes no workspace
+ * argument: the per-range partial results go to a 64 MiB array built into
+ * this library, which every GPU that loads the library holds until the
+ * process exits. Nothing here allocates memory.
+ *   Arguments as attn_fwd_splitkv without workspace / workspace_bytes.
+ *   The workspace the call needs, num_splits' * B * Hq * Sq * (d + 1) * 4
+ *   bytes (num_splits' = the non-empty ranges), must not exceed 64 MiB;
+ *   larger requests return ATTN_ERR_INVALID_ARG without launching anything.
+ *   The first call on a device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture.
+ *   Every call on a device shares the one array and it keeps the last call's
+ *   contents; nothing in it needs clearing (each call writes every entry it
+ *   reads), but calls whose kernels overlap on the GPU (other streams, other
+ *   host threads) race on it: serialise them.
+ * There is no counterpart on the source pages: this entry point exists only
+ * for callers that cannot allocate. Returns an attn_status_t.
+ */
+int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* o, float* lse,
+                             int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal,
+                             float scale, int dtype, int num_splits, attn_stream_t stream);
+
+/*
  * attn_quantize_fp8_e4m3 -- block quantiser producing attn_fwd_fp8 inputs
  * (same section of the FlashAttention-3 deep dive: per-block scale from the
  * block's local maximum).
