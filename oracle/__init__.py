@@ -55,6 +55,10 @@ def _load():
         lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
         lib.oracle_quantize_fp8_e4m3.restype = None
         lib.oracle_quantize_fp8_e4m3.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 4
+        lib.oracle_rmsnorm_heads.restype = None
+        lib.oracle_rmsnorm_heads.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                             ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
+                                             ctypes.c_int, ctypes.c_double]
         lib.oracle_attn_fwd.restype = ctypes.c_int
         lib.oracle_attn_fwd.argtypes = (
             [ctypes.c_void_p] * 6 + [ctypes.c_int] + [ctypes.c_void_p] * 2
@@ -102,6 +106,24 @@ def quantize_fp8_e4m3(x: np.ndarray):
     scales = np.empty((B, H, nblk), dtype=np.float32)
     _load().oracle_quantize_fp8_e4m3(_ptr(x), _ptr(codes), _ptr(scales), B, S, H, d)
     return codes, scales
+
+
+def rmsnorm_heads(x, w, eps: float, dtype: str = "bf16"):
+    """fp64 RMSNorm across heads of x [..., H, d] (16-bit bits as uint16) with
+    weight w [H * d] (same type): every token's H * d values share one RMS.
+    Returns fp64 with x's shape."""
+    if dtype not in ("bf16", "f16"):
+        raise ValueError(f"unknown dtype {dtype!r}")
+    x = np.ascontiguousarray(x).view(np.uint16)
+    w = np.ascontiguousarray(w).view(np.uint16)
+    H, d = x.shape[-2], x.shape[-1]
+    if w.size != H * d:
+        raise ValueError("w must hold H * d weights")
+    T = x.size // (H * d)
+    y = np.empty(x.shape, dtype=np.float64)
+    _load().oracle_rmsnorm_heads(_ptr(x), _ptr(w), DTYPE_F16 if dtype == "f16" else DTYPE_BF16,
+                                 _ptr(y), T, H, d, float(eps))
+    return y
 
 
 def attn_fwd(q, k, v, causal: bool, scale: float, dtype: str = "bf16",

@@ -154,6 +154,38 @@ void oracle_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scales,
             }
 }
 
+/* --------------------------------------------------- QK RMSNorm (heads) -- */
+
+/* "QKNorm across heads" (SGLang PR 21503 analysis, secrett2633 blog): RMSNorm
+ * of each token's whole hidden vector, all heads together, before attention:
+ *     y[t, h, c] = x[t, h, c] / sqrt(eps + (1/(H d)) sum_{h', c'} x[t, h', c']^2)
+ *                  * w[h d + c]
+ * x: [T, H, d] 16-bit bits (bf16 or IEEE fp16, `dtype`), w: [H d] same type.
+ * y: fp64 [T, H, d] (not rounded; the caller compares against its own
+ * rounding). Q and K are normalised independently with their own weights. */
+void oracle_rmsnorm_heads(const uint16_t* x, const uint16_t* w, int dtype, double* y,
+                          long long T, int H, int d, double eps) {
+    const long long n = (long long)H * d;
+#pragma omp parallel for schedule(static)
+    for (long long t = 0; t < T; ++t) {
+        const uint16_t* row = x + t * n;
+        double ss = 0.0;
+        for (long long i = 0; i < n; ++i) {
+            double v = dtype == ORACLE_DTYPE_F16 ? oracle_f16_decode(row[i])
+                                                 : bf16_bits_to_double(row[i]);
+            ss += v * v;
+        }
+        const double r = 1.0 / sqrt(eps + ss / (double)n);
+        for (long long i = 0; i < n; ++i) {
+            double v = dtype == ORACLE_DTYPE_F16 ? oracle_f16_decode(row[i])
+                                                 : bf16_bits_to_double(row[i]);
+            double wi = dtype == ORACLE_DTYPE_F16 ? oracle_f16_decode(w[i])
+                                                  : bf16_bits_to_double(w[i]);
+            y[t * n + i] = v * r * wi;
+        }
+    }
+}
+
 /* ------------------------------------------------------------ attention -- */
 
 typedef struct {

@@ -361,3 +361,53 @@ def test_merging_key_ranges_reproduces_the_whole(oracle_mod):
         w2 = np.exp(l2 - lm).transpose(0, 2, 1)[..., None]
         np.testing.assert_allclose(lm, lse, rtol=0, atol=1e-12)
         np.testing.assert_allclose(w1 * o1 + w2 * o2, o, rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------- QK RMSNorm (heads) --
+
+def _bits(x, dtype):
+    t = torch.tensor(np.asarray(x, dtype=np.float32),
+                     dtype=torch.float16 if dtype == "f16" else torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16), t.to(torch.float64).numpy()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+def test_rmsnorm_heads_brute_force(oracle_mod, dtype):
+    rng = np.random.default_rng(31)
+    T, H, d, eps = 5, 3, 4, 1e-6
+    xb, xv = _bits(rng.standard_normal((T, H, d)) * 3, dtype)
+    wb, wv = _bits(rng.standard_normal(H * d), dtype)
+    y = oracle_mod.rmsnorm_heads(xb, wb, eps, dtype)
+    for t in range(T):
+        vals = [float(v) for v in xv[t].ravel()]
+        r = 1.0 / math.sqrt(eps + sum(v * v for v in vals) / len(vals))
+        want = [vals[i] * r * float(wv[i]) for i in range(len(vals))]
+        np.testing.assert_allclose(y[t].ravel(), want, rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_heads_closed_forms(oracle_mod):
+    # a constant row c with unit weights and eps = 0 normalises to sign(c)
+    xb, _ = _bits(np.full((2, 4, 8), -2.5), "bf16")
+    wb, _ = _bits(np.ones(32), "bf16")
+    np.testing.assert_array_equal(oracle_mod.rmsnorm_heads(xb, wb, 0.0), -np.ones((2, 4, 8)))
+    # with unit weights and eps = 0 every row has mean square 1, whatever its scale
+    rng = np.random.default_rng(5)
+    for s in (1e-3, 1.0, 300.0):
+        xb, _ = _bits(rng.standard_normal((3, 2, 64)) * s, "bf16")
+        wb, _ = _bits(np.ones(128), "bf16")
+        y = oracle_mod.rmsnorm_heads(xb, wb, 0.0)
+        np.testing.assert_allclose((y ** 2).mean(axis=(1, 2)), 1.0, rtol=1e-12)
+
+
+def test_rmsnorm_heads_spans_all_heads(oracle_mod):
+    """Across heads, not per head: scaling one head's values changes the
+    normalisation of every head in the token."""
+    rng = np.random.default_rng(9)
+    x = rng.standard_normal((1, 4, 16))
+    wb, _ = _bits(np.ones(64), "bf16")
+    y0 = oracle_mod.rmsnorm_heads(_bits(x, "bf16")[0], wb, 1e-6)
+    x2 = x.copy()
+    x2[0, 0] *= 4.0  # exact in bf16
+    y1 = oracle_mod.rmsnorm_heads(_bits(x2, "bf16")[0], wb, 1e-6)
+    ratio = y1[0, 1:] / y0[0, 1:]
+    assert np.allclose(ratio, ratio.flat[0]) and ratio.flat[0] < 0.9
