@@ -318,8 +318,28 @@ def run_ours(args, w):
         wbytes = nsplit * w.B * w.Hq * w.Sq * (w.d + 1) * 4
         ws = torch.empty(wbytes // 4, dtype=torch.float32, device=dev)
 
+    norm = None
+    if w.qknorm:
+        wq = inputs.draw_norm_weights(w.Hq * w.d, w.seed + 50, w.dtype).to(dev)
+        wk = inputs.draw_norm_weights(w.Hkv * w.d, w.seed + 51, w.dtype).to(dev)
+        norm = (wq, wk, torch.empty_like(dev_in[0]), torch.empty_like(dev_in[1]))
+
+    def prologue():
+        q, k, _ = dev_in[:3]
+        wq, wk, qn, kn = norm
+        rc = ea.attn_qk_rmsnorm(q, k, wq, wk, qn, kn, w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.d, 1e-6,
+                                ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
+        if rc != ea.ATTN_OK:
+            raise ea.AttnError(rc, "attn_qk_rmsnorm")
+        return qn, kn
+
     def step():
-        if ws is not None:
+        if norm is not None:
+            qn, kn = prologue()
+            rc = ea.attn_fwd(qn, kn, dev_in[2], o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
+                             w.causal, w.scale,
+                             ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
+        elif ws is not None:
             q, k, v = dev_in
             rc = ea.attn_fwd_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
                                      w.causal, w.scale,
@@ -403,6 +423,29 @@ def run_ours(args, w):
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms / e_steps}
 
+    prologue_line = None
+    if norm is not None:
+        # the RMSNorm kernel on its own (HBM-bound): algorithmic bytes = Q and K
+        # read and written once, plus the weights
+        p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 50
+        prologue()
+        torch.cuda.synchronize(dev)
+        p0.record(stream)
+        for _ in range(reps):
+            prologue()
+        p1.record(stream)
+        torch.cuda.synchronize(dev)
+        pms = p0.elapsed_time(p1) / reps
+        nbytes = 2 * 2 * (w.B * w.Sq * w.Hq * w.d + w.B * w.Sk * w.Hkv * w.d) + \
+            2 * (w.Hq + w.Hkv) * w.d
+        peaks_p, src_p = load_peaks()
+        gbs = nbytes / (pms * 1e-3) / 1e9
+        prologue_line = {"kernel": "qk_rmsnorm_kernel", "ms": pms, "bound": "hbm",
+                         "achieved": gbs, "peak": peaks_p["hbm_gbs"], "unit": "GB/s",
+                         "frac": gbs / peaks_p["hbm_gbs"], "bytes": nbytes,
+                         "peak_source": f"{src_p} hbm copy"}
+
     if rank != 0:
         if dist is not None:
             dist.destroy_process_group()
@@ -429,8 +472,11 @@ def run_ours(args, w):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, nsplit), "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": args.steps * (2 if ws is not None else 1), "roofline": roofline,
+        "gpu_launches": args.steps * (2 if (ws is not None or norm is not None) else 1),
+        "roofline": roofline,
     }
+    if prologue_line is not None:
+        line["prologue"] = prologue_line
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)

@@ -20,7 +20,7 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
     "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "ATTN_F16", "AttnError",
     "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc",
-    "attn_splitkv_plan",
+    "attn_splitkv_plan", "attn_qk_rmsnorm", "qk_rmsnorm",
     "attn_quantize_fp8_e4m3", "attn_device_status",
     "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
     "library_path", "load",
@@ -78,6 +78,8 @@ def load():
         lib.attn_splitkv_plan.argtypes = [I, I, I, I, I, I, I, ctypes.POINTER(I),
                                           ctypes.POINTER(ctypes.c_size_t)]
         lib.attn_splitkv_plan.restype = I
+        lib.attn_qk_rmsnorm.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, F, I, P]
+        lib.attn_qk_rmsnorm.restype = I
         lib.attn_quantize_fp8_e4m3.argtypes = [P, P, P, I, I, I, I, P]
         lib.attn_quantize_fp8_e4m3.restype = I
         lib.attn_device_status.argtypes = [P]
@@ -148,6 +150,13 @@ def attn_splitkv_plan(B, Hq, Sq, Sk, d, causal=False, num_sms=0):
     rc = load().attn_splitkv_plan(int(B), int(Hq), int(Sq), int(Sk), int(d), int(bool(causal)),
                                   int(num_sms), ctypes.byref(n), ctypes.byref(w))
     return rc, n.value, w.value
+
+
+def attn_qk_rmsnorm(q, k, q_weight, k_weight, q_out, k_out, B, Sq, Sk, Hq, Hkv, d, eps, dtype,
+                    stream=None) -> int:
+    return load().attn_qk_rmsnorm(_ptr(q), _ptr(k), _ptr(q_weight), _ptr(k_weight), _ptr(q_out),
+                                  _ptr(k_out), int(B), int(Sq), int(Sk), int(Hq), int(Hkv),
+                                  int(d), float(eps), int(dtype), _stream(stream))
 
 
 def attn_quantize_fp8_e4m3(x, codes, scale, B, S, H, d, stream=None) -> int:
@@ -242,6 +251,20 @@ def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                             num_splits, workspace, workspace.numel() * workspace.element_size(),
                             stream), "attn_fwd_splitkv")
     return out, lse
+
+
+def qk_rmsnorm(q, k, q_weight, k_weight, eps: float = 1e-6, out=None, stream=None):
+    """RMSNorm across heads of q [B,Sq,Hq,d] and k [B,Sk,Hkv,d] (bf16 or fp16,
+    CUDA) with weights [Hq*d] / [Hkv*d]. out = (q_out, k_out), or None for new
+    tensors; pass (q, k) to normalise in place. Returns (q_out, k_out)."""
+    import torch
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    code = ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16
+    q_out, k_out = out if out is not None else (torch.empty_like(q), torch.empty_like(k))
+    _check(attn_qk_rmsnorm(q, k, q_weight, k_weight, q_out, k_out, B, Sq, Sk, Hq, Hkv, d, eps,
+                           code, stream), "attn_qk_rmsnorm")
+    return q_out, k_out
 
 
 def quantize_fp8(x, stream=None):

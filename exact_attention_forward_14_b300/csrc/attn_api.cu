@@ -16,6 +16,7 @@
 #include "attn_b300.h"
 #include "attn_fwd_kernel.cuh"
 #include "quantize_fp8.cuh"
+#include "qk_rmsnorm.cuh"
 #include "splitkv_combine.cuh"
 #include "tmap.cuh"
 
@@ -356,6 +357,42 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
   if (rc != ATTN_OK) return rc;
   return attn_fwd_splitkv(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype,
                           num_splits, scratch, kNoAllocScratchBytes, stream);
+}
+
+int attn_qk_rmsnorm(const void* q, const void* k, const void* q_weight, const void* k_weight,
+                    void* q_out, void* k_out, int B, int Sq, int Sk, int Hq, int Hkv, int d,
+                    float eps, int dtype, attn_stream_t stream) {
+  if (!q || !k || !q_weight || !k_weight || !q_out || !k_out) return ATTN_ERR_INVALID_ARG;
+  if (B <= 0 || Sq <= 0 || Sk <= 0 || Hq <= 0 || Hkv <= 0 || d <= 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(eps) || eps < 0.f) return ATTN_ERR_INVALID_ARG;
+  if (!fits_i32(B, Sq, Hq, d) || !fits_i32(B, Sk, Hkv, d)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+  for (const void* p : {q, k, q_weight, k_weight, static_cast<const void*>(q_out),
+                        static_cast<const void*>(k_out)})
+    if (!aligned(p, 16)) return ATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  int rc = current_device(&di);
+  if (rc != ATTN_OK) return rc;
+  const long long tq = static_cast<long long>(B) * Sq, tk = static_cast<long long>(B) * Sk;
+  const long long tmax = tq > tk ? tq : tk;
+  const long long blocks = (tmax + attnb3::NORM_TOKENS_PER_BLOCK - 1) / attnb3::NORM_TOKENS_PER_BLOCK;
+  if (blocks > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
+  const dim3 grid(static_cast<unsigned>(blocks), 2);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  auto* qo = static_cast<uint16_t*>(q_out);
+  auto* ko = static_cast<uint16_t*>(k_out);
+  auto* qi = static_cast<const uint16_t*>(q);
+  auto* ki = static_cast<const uint16_t*>(k);
+  auto* wq = static_cast<const uint16_t*>(q_weight);
+  auto* wk = static_cast<const uint16_t*>(k_weight);
+  if (dtype == ATTN_F16)
+    attnb3::qk_rmsnorm_kernel<true><<<grid, attnb3::NORM_THREADS, 0, st>>>(
+        qi, ki, wq, wk, qo, ko, tq, tk, Hq * d, Hkv * d, eps);
+  else
+    attnb3::qk_rmsnorm_kernel<false><<<grid, attnb3::NORM_THREADS, 0, st>>>(
+        qi, ki, wq, wk, qo, ko, tq, tk, Hq * d, Hkv * d, eps);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, int S, int H,

@@ -37,6 +37,7 @@ class Workload:
     outlier_frac: float = 0.0
     seed: int = 1000
     splits: int = 0              # split-KV ranges: 0 = plain forward, -1 = the plan's choice
+    qknorm: bool = False         # RMSNorm across heads of Q and K before the attention
 
     @property
     def scale(self) -> float:
@@ -68,6 +69,9 @@ WORKLOADS = {
     "longkv_b1hq32hkv8sq256sk65536d128_splitkv": Workload(
         "longkv_b1hq32hkv8sq256sk65536d128_splitkv", 1, 32, 8, 256, 65536, 128, False,
         seed=1006, splits=-1),
+    # the long-context prefill shape behind the QK-RMSNorm prologue
+    "qknorm_b2h32s8192d128_causal": Workload("qknorm_b2h32s8192d128_causal", 2, 32, 32, 8192,
+                                             8192, 128, True, seed=1002, qknorm=True),
     # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
     "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
                                           True, dtype="f16", seed=1005),
@@ -107,6 +111,13 @@ def draw_workload_16(w: Workload):
     """The workload's q, k, v in its 16-bit type (bf16 or f16)."""
     f = draw_qkv_f16 if w.dtype == "f16" else draw_qkv_bf16
     return f(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
+
+
+def draw_norm_weights(n, seed, dtype="bf16"):
+    """RMSNorm weights ~ 1 + 0.25 N(0, 1), rounded to the 16-bit type."""
+    g = torch.Generator().manual_seed(int(seed))
+    w = 1.0 + 0.25 * torch.randn(n, generator=g)
+    return w.to(torch.float16 if dtype == "f16" else torch.bfloat16)
 
 
 def bits16(t: torch.Tensor) -> np.ndarray:

@@ -169,6 +169,28 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              float scale, int dtype, int num_splits, attn_stream_t stream);
 
 /*
+ * attn_qk_rmsnorm -- the attention prologue "QKNorm across heads" (SGLang PR
+ * 21503 analysis on the secrett2633 blog): RMSNorm of Q and of K in which each
+ * token's whole hidden vector (all heads x d) shares one RMS:
+ *     y[b, s, h, c] = x[b, s, h, c] * w[h * d + c]
+ *                     / sqrt(eps + mean over (h', c') of x[b, s, h', c']^2)
+ *   q, k       : device inputs [B, Sq, Hq, d] and [B, Sk, Hkv, d]
+ *   q_weight,
+ *   k_weight   : device weights [Hq * d] and [Hkv * d]
+ *   q_out,
+ *   k_out      : device outputs, same shapes as q and k; may be q and k
+ *                themselves (in place), must not otherwise overlap them
+ *   eps        : finite, >= 0
+ *   dtype      : ATTN_BF16 or ATTN_F16, for every tensor here
+ * Arithmetic in fp32, y rounded to nearest in the storage type. All pointers
+ * 16-byte aligned; d in {64, 128}. One kernel on `stream`. Returns an
+ * attn_status_t (ATTN_ERR_UNSUPPORTED for other dtypes or d).
+ */
+int attn_qk_rmsnorm(const void* q, const void* k, const void* q_weight, const void* k_weight,
+                    void* q_out, void* k_out, int B, int Sq, int Sk, int Hq, int Hkv, int d,
+                    float eps, int dtype, attn_stream_t stream);
+
+/*
  * attn_quantize_fp8_e4m3 -- block quantiser producing attn_fwd_fp8 inputs
  * (same section of the FlashAttention-3 deep dive: per-block scale from the
  * block's local maximum).

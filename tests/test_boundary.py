@@ -182,3 +182,25 @@ def test_splitkv_rejects_bad_arguments(lib, kw, code):
                              a["causal"], a["scale"], a["dtype"], a["num_splits"], a["workspace"],
                              a["workspace_bytes"], stream=0)
     assert rc == code
+
+
+# --------------------------------------------------------------- QK RMSNorm --
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(q=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(k_out=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(B=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(eps=-1.0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(eps=float("nan")), ea.ATTN_ERR_INVALID_ARG),
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(dtype=ea.ATTN_FP8_E4M3), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(q_weight=0x70004), ea.ATTN_ERR_MISALIGNED),
+])
+def test_qk_rmsnorm_rejects_bad_arguments(lib, kw, code):
+    a = dict(q=Q, k=K, q_weight=0x70000, k_weight=0x80000, q_out=O, k_out=0x90000, B=1, Sq=8,
+             Sk=8, Hq=2, Hkv=2, d=64, eps=1e-6, dtype=ea.ATTN_BF16)
+    a.update(kw)
+    rc = ea.attn_qk_rmsnorm(a["q"], a["k"], a["q_weight"], a["k_weight"], a["q_out"], a["k_out"],
+                            a["B"], a["Sq"], a["Sk"], a["Hq"], a["Hkv"], a["d"], a["eps"],
+                            a["dtype"], stream=0)
+    assert rc == code
