@@ -376,7 +376,7 @@ int attn_qk_rmsnorm(const void* q, const void* k, const void* q_weight, const vo
   if (rc != ATTN_OK) return rc;
   const long long tq = static_cast<long long>(B) * Sq, tk = static_cast<long long>(B) * Sk;
   const long long tmax = tq > tk ? tq : tk;
-  const long long blocks = (tmax + attnb3::NORM_TOKENS_PER_BLOCK - 1) / attnb3::NORM_TOKENS_PER_BLOCK;
+  const long long blocks = tmax;  // one block per token
   if (blocks > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
   const dim3 grid(static_cast<unsigned>(blocks), 2);
   const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
