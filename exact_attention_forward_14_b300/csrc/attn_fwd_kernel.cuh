@@ -88,6 +88,7 @@ struct FwdParams {
   // lse. nsplit = 1, kps = nkv, o_part = null is the plain forward pass.
   int nsplit;
   int kps;
+  int lpt;          // 1: longest-first unit order (see cta_unit)
   float* o_part;    // [nsplit, B, Hq, Sq, d] fp32
   float* lse_part;  // [nsplit, B, Hq, Sq] fp32
   float scale_log2;  // softmax scale * log2(e)
@@ -209,23 +210,28 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 
 // Work items and units. A unit is (b, hq, 256 query rows); the units of one
 // (b, hq) are its n_qp "levels" (level L covers rows [256 L, 256 L + 256)).
-// A work item pairs level n_qp-1-p with level p of the same (b, hq), so under
-// a causal mask every item costs the same number of K/V tiles (a heavy unit
-// plus its mirror) and a static round-robin over items balances the CTAs.
-// Items are numbered (b, hq)-major with hq fastest: the CTAs running at the
-// same time cover only a few heads (query heads sharing a KV head are
-// adjacent), so those heads' K/V tiles are re-read from L2, not HBM.
-// With split-KV, item w covers key range w % nsplit of pair w / nsplit.
-// Returns false when item w has no k-th unit (odd n_qp, middle level).
-__device__ __forceinline__ bool decode_unit(int w, int k, const FwdParams& P, Unit& U) {
-  U.split = w % P.nsplit;
-  w /= P.nsplit;
-  U.j0 = U.split * P.kps;
+//
+// Pair order (the default): a work item pairs level n_qp-1-p with level p of
+// the same (b, hq), so under a causal mask every item costs the same number
+// of K/V tiles (a heavy unit plus its mirror) and a static round-robin over
+// items balances the CTAs. Items are numbered (b, hq)-major with hq fastest:
+// the CTAs running at the same time cover only a few heads (query heads
+// sharing a KV head are adjacent), so those heads' K/V tiles are re-read from
+// L2, not HBM. With split-KV, item w covers key range w % nsplit of pair
+// w / nsplit.
+//
+// Longest-first order (lpt != 0; chosen by the host when there are fewer
+// than 4 items per CTA, where whole items leave the last round part-empty):
+// single units sorted by level, highest (most K/V tiles) first, dealt to the
+// CTAs in a snake (round r goes left to right for even r, right to left for
+// odd r), which evens out the per-CTA totals.
+
+// Fills U for unit (level, bh, split); the key range is split's K/V tiles.
+__device__ __forceinline__ void fill_unit(int level, int bh, int split, const FwdParams& P,
+                                          Unit& U) {
+  U.split = split;
+  U.j0 = split * P.kps;
   const int j1 = min(U.j0 + P.kps, P.nkv);
-  const int bh = w / P.npair;
-  const int p = w - bh * P.npair;
-  const int level = k == 0 ? P.n_qp - 1 - p : p;
-  if (k == 1 && level == P.n_qp - 1 - p) return false;
   U.b = bh / P.Hq;
   U.hq = bh - U.b * P.Hq;
   U.hkv = U.hq / P.group;
@@ -246,7 +252,30 @@ __device__ __forceinline__ bool decode_unit(int w, int k, const FwdParams& P, Un
     U.n[t] = max(0, min(n, j1) - U.j0);
   }
   U.nmax = max(U.n[0], U.n[1]);
-  return true;
+}
+
+// The i-th unit of this CTA: 0 = no more units, 1 = nothing at this position
+// (skip it), 2 = U filled.
+__device__ __forceinline__ int cta_unit(int i, const FwdParams& P, Unit& U) {
+  const int G = gridDim.x, c = blockIdx.x;
+  if (P.lpt) {
+    const int kg = i * G + ((i & 1) ? G - 1 - c : c);
+    const int bh_count = P.B * P.Hq;
+    if (kg >= bh_count * P.n_qp) return 0;
+    fill_unit(P.n_qp - 1 - kg / bh_count, kg % bh_count, 0, P, U);
+    return 2;
+  }
+  int w = c + (i >> 1) * G;
+  const int k = i & 1;
+  if (w >= P.num_items) return 0;
+  const int split = w % P.nsplit;
+  w /= P.nsplit;
+  const int bh = w / P.npair;
+  const int p = w - bh * P.npair;
+  const int level = k == 0 ? P.n_qp - 1 - p : p;
+  if (k == 1 && level == P.n_qp - 1 - p) return 1;  // odd n_qp: the middle level
+  fill_unit(level, bh, split, P, U);
+  return 2;
 }
 
 struct Ctl {
@@ -349,9 +378,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       uint32_t it = 0, qit = 0;
       bool ok = true;
-      for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+      for (int i = 0; ok; ++i) {
         Unit U;
-        if (!decode_unit(u >> 1, u & 1, P, U) || U.nmax == 0) continue;
+        const int st = cta_unit(i, P, U);
+        if (st == 0) break;
+        if (st == 1 || U.nmax == 0) continue;
         if (!wait_bounded(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
 #ifndef ATTN_TEST_NEVER_ARM_Q
         const int nq = (U.n[0] > 0) + (U.n[1] > 0);
@@ -415,9 +446,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                               kv_smem + slot * C::KV_TILE_BYTES, half, acc);
       };
 
-      for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+      for (int i = 0; ok; ++i) {
         Unit U;
-        if (!decode_unit(u >> 1, u & 1, P, U) || U.nmax == 0) continue;
+        const int st = cta_unit(i, P, U);
+        if (st == 0) break;
+        if (st == 1 || U.nmax == 0) continue;
         if (!wait_bounded(BAR_Q_FULL, qit & 1u, ctl, P)) { ok = false; break; }
         tc_fence_after();
         {
@@ -490,9 +523,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t sc = 0, oc = 0;  // phase counters of s_full[t], o_full[t]
     bool ok = true;
 
-    for (int u = 2 * blockIdx.x; ok && u < 2 * P.num_items; u += (u & 1) ? 2 * gridDim.x - 1 : 1) {
+    for (int i = 0; ok; ++i) {
       Unit U;
-      if (!decode_unit(u >> 1, u & 1, P, U)) continue;
+      const int st = cta_unit(i, P, U);
+      if (st == 0) break;
+      if (st == 1) continue;
       const int tile_row0 = U.row0 + t * BM;
       if (tile_row0 >= P.Sq) continue;  // idle tile
       const int row = tile_row0 + rloc;
