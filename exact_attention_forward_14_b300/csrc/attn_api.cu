@@ -146,7 +146,7 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
   P.lpt = (P.nsplit == 1 && P.num_items < 4 * di->num_sms) ? 1 : 0;
   const int work = P.lpt ? B * Hq * P.n_qp : P.num_items;
   const int grid = work < di->num_sms ? work : di->num_sms;
-  kern<<<grid, attnb3::NUM_THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
+  kern<<<grid, C::THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

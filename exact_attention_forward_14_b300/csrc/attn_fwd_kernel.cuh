@@ -23,12 +23,16 @@
 //   warps 4-7  softmax for Q tile 1 (ping-pong partner of tile 0)
 //   warp  8    MMA issuer (lane 0) and TMEM owner
 //   warp  9    TMA producer (lane 0)
+//   warps 10-11 (E4M3 inputs only, 384 threads) widen each staged E4M3 V
+//              tile to fp16 in one of two shared-memory buffers: S = Q K^T
+//              runs on E4M3 operands, O += P V on fp16 ones, P kept in fp16
+//              (both MMA operands must share one element type)
 // A work unit is (b, hq, 256 query rows) = two 128-row Q tiles that share one
 // stream of 128-key K/V tiles. Per K/V tile j the MMA warp issues, in order,
 //   O0 += P0(j) V(j);  S0(j+1) = Q0 K(j+1)^T;  O1 += P1(j) V(j);  S1(j+1) = ...
 // so while softmax 0 works on S0(j+1) the tensor cores run tile 1's MMAs and
-// vice versa. P(j) overwrites the low columns of S(j) in TMEM (bf16 pairs or
-// E4M3 quads per 32-bit column); in-order execution of MMAs from one thread
+// vice versa. P(j) overwrites the low columns of S(j) in TMEM (bf16 or fp16
+// pairs per 32-bit column); in-order execution of MMAs from one thread
 // makes S(j+1) wait for P(j)'s consumer.
 //
 // TMEM columns (512 allocated): S0 [0,128) S1 [128,256) O0 [256,256+d)
@@ -51,20 +55,19 @@
 #include <cstdint>
 
 #include "ptx.cuh"
+#include "widen_v.cuh"
 
 namespace attnb3 {
 
 constexpr int BM = 128;           // query rows per Q tile
 constexpr int BN = 128;           // keys per K/V tile
 constexpr int UNIT_ROWS = 2 * BM; // query rows per work unit
-constexpr int NUM_THREADS = 320;
+constexpr int NUM_THREADS = 320;      // bf16 / fp16
+constexpr int NUM_THREADS_FP8 = 384;  // + warps 10-11 widening V to fp16
+constexpr int WARP_WIDEN = 10;        // first of the two V-widening warps
 constexpr int WARP_MMA = 8;
 constexpr int WARP_LOAD = 9;
 constexpr float RESCALE_LOG2 = 8.0f;
-// FP8: P is written as p * 2^P_SCALE_LOG2 * (V block scale / largest V block
-// scale), so with p <= 2^4 the largest value is 256 and the lo part of the
-// split stays clear of the E4M3 subnormal range for every weight that matters.
-constexpr float P_SCALE_LOG2 = 4.0f;
 constexpr float LN2 = 0.6931471805599453f;
 constexpr int STATUS_TIMEOUT = 5;  // ATTN_ERR_TIMEOUT
 constexpr int FP8_BLOCK = 64;      // rows per FP8 scale block
@@ -111,30 +114,38 @@ struct Cfg {
   static constexpr int NSLOT = KV_TILE_BYTES >= 32768 ? 4 : 8;
   static constexpr int MMA_K = FP8 ? 32 : 16;  // 32 bytes of K per instruction
   static constexpr int KSTEPS_QK = D / MMA_K;
-  static constexpr int KSTEPS_PV = BN / MMA_K;
-  static constexpr int P_COLS = BN * ESZ / 4;  // TMEM columns holding one P part
-  static constexpr int P_COLS_PER_KSTEP = MMA_K * ESZ / 4;
-  // FP8 keeps P to about 8 significant bits as two E4M3 parts (hi, lo), each
-  // multiplied by the same V tile; bf16 P is one part.
-  static constexpr int P_PARTS = FP8 ? 2 : 1;
-  // Stale-max threshold (log2 units): p <= 2^RESCALE before any scaling. FP8
-  // uses a lower one so p * P_SCALE stays inside the E4M3 range (<= 448).
-  static constexpr float RESCALE = FP8 ? 4.0f : RESCALE_LOG2;
-  static_assert(P_PARTS * P_COLS <= BN, "P parts must fit in the S columns");
+  // O += P V always runs on 16-bit operands: P is bf16 or fp16 (fp16 for
+  // FP8 inputs, whose V tiles are widened to fp16 in shared memory first).
+  static constexpr int KSTEPS_PV = BN / 16;
+  static constexpr int P_COLS = BN * 2 / 4;  // TMEM columns holding P
+  static constexpr int P_COLS_PER_KSTEP = 16 * 2 / 4;
+  static constexpr int P_PARTS = 1;
+  static constexpr float RESCALE = RESCALE_LOG2;  // stale-max threshold, log2 units
+  static_assert(P_COLS <= BN, "P must fit in the S columns");
+  static constexpr int THREADS = FP8 ? NUM_THREADS_FP8 : NUM_THREADS;
+  static constexpr int V16_TILE_BYTES = BN * D * 2;  // FP8: a widened V tile
   // operand format: kind::f8f6f4 0 = e4m3; kind::f16 0 = f16, 1 = bf16
   static constexpr uint32_t AB_FMT = (FP8 || F16) ? 0u : 1u;
   static constexpr uint32_t IDESC_S = make_idesc(BM, BN, AB_FMT, false);
-  static constexpr uint32_t IDESC_PV = make_idesc(BM, D, AB_FMT, true);
+  static constexpr uint32_t IDESC_PV = make_idesc(BM, D, (FP8 || F16) ? 0u : 1u, true);
+  // the V operand of O += P V (FP8: the widened fp16 tile)
+  static constexpr int V_CHUNK_BYTES = 128;            // 128-byte swizzle span
+  static constexpr int V_KV_CHUNK_BYTES = BN * V_CHUNK_BYTES;
   static constexpr int COL_S0 = 0;
   static constexpr int COL_O0 = 2 * BN;
   static constexpr int TMEM_COLS = 512;
   // shared memory (offsets from a 1024-byte aligned base)
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_KV = 2 * Q_TILE_BYTES;
-  static constexpr int OFF_BAR = OFF_KV + NSLOT * KV_TILE_BYTES;
+  static constexpr int OFF_VF = OFF_KV + NSLOT * KV_TILE_BYTES;  // FP8: 2 widened V tiles
+  static constexpr int OFF_BAR = OFF_VF + (FP8 ? 2 * V16_TILE_BYTES : 0);
   // barriers: q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2],
-  // p_full[2 tiles][2 halves], o_full[2], drain
-  static constexpr int NUM_BARS = 2 + 2 * NSLOT + 9;
+  // p_full[2 tiles][2 halves], o_full[2], drain, vf_full[2], vf_empty[2]
+  static constexpr int NUM_BARS = 2 + 2 * NSLOT + 13;
+  // K and V fills alternate, so with an even ring K always lands in even
+  // slots and V in odd ones (the FP8 path releases V slots from the widening
+  // warps, K slots from the MMA thread)
+  static_assert(NSLOT % 2 == 0, "K/V slots alternate");
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
   static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
   // Launch with the whole opt-in budget (one CTA per SM either way), so a
@@ -166,28 +177,24 @@ __device__ __forceinline__ void issue_qk(uint32_t d_tmem, uint32_t q_smem, uint3
 }
 
 // O (+)= P V for one half of the K/V tile (keys [64 h, 64 h + 64)): P
-// (128 x 128 keys) in tensor memory, packed along the keys (FP8: the hi part
-// in the first P_COLS columns, the lo part after it); V tile staged by TMA
-// with d contiguous (MN-major B operand): the leading byte offset steps
-// between d-chunks, the stride byte offset between groups of 8 keys; each
-// instruction consumes MMA_K keys. `accumulate` = false starts O afresh.
+// (128 x 128 keys, bf16 or fp16) in tensor memory, packed along the keys; the
+// 16-bit V tile (staged by TMA, or for FP8 inputs widened to fp16 in shared
+// memory) has d contiguous in 128-byte swizzled chunks (MN-major B operand):
+// the leading byte offset steps between d-chunks, the stride byte offset
+// between groups of 8 keys; each instruction consumes 16 keys. `accumulate`
+// = false starts O afresh.
 template <int D, bool FP8, bool F16 = false>
 __device__ __forceinline__ void issue_pv_half(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
                                               int half, bool accumulate) {
   using C = Cfg<D, FP8, F16>;
   constexpr int KS_HALF = C::KSTEPS_PV / 2;
 #pragma unroll
-  for (int part = 0; part < C::P_PARTS; ++part) {
-#pragma unroll
-    for (int k = 0; k < KS_HALF; ++k) {
-      const int ks = half * KS_HALF + k;
-      const uint64_t b = make_sdesc(v_smem + ks * C::MMA_K * C::CHUNK_BYTES, C::KV_CHUNK_BYTES,
-                                    8 * C::CHUNK_BYTES, C::SWZ_CODE);
-      const uint32_t a = p_tmem + part * C::P_COLS + ks * C::P_COLS_PER_KSTEP;
-      const uint32_t acc = (accumulate || part > 0 || ks > 0) ? 1u : 0u;
-      if constexpr (FP8) mma_f8_ts(d_tmem, a, b, C::IDESC_PV, acc);
-      else mma_f16_ts(d_tmem, a, b, C::IDESC_PV, acc);
-    }
+  for (int k = 0; k < KS_HALF; ++k) {
+    const int ks = half * KS_HALF + k;
+    const uint64_t b = make_sdesc(v_smem + ks * 16 * C::V_CHUNK_BYTES, C::V_KV_CHUNK_BYTES,
+                                  8 * C::V_CHUNK_BYTES, 2u);
+    const uint32_t a = p_tmem + ks * C::P_COLS_PER_KSTEP;
+    mma_f16_ts(d_tmem, a, b, C::IDESC_PV, (accumulate || ks > 0) ? 1u : 0u);
   }
 }
 
@@ -317,7 +324,7 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const 
 // F16: q, k, v and o are fp16 (P is packed as f16 too); otherwise 16-bit
 // data is bf16 and FP8 inputs produce a bf16 O.
 template <int D, bool FP8, bool F16>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q,
                     const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const FwdParams P) {
@@ -336,6 +343,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const uint32_t BAR_P_FULL = BAR_S_FULL + 16;                // + 16 * t + 8 * half
   const uint32_t BAR_O_FULL = BAR_P_FULL + 32;                // + 8 * t
   const uint32_t BAR_DRAIN = BAR_O_FULL + 16;
+  const uint32_t BAR_VF_FULL = BAR_DRAIN + 8;                 // + 8 * buffer (FP8)
+  const uint32_t BAR_VF_EMPTY = BAR_VF_FULL + 16;             // + 8 * buffer (FP8)
   volatile Ctl* ctl = reinterpret_cast<volatile Ctl*>(smem + C::OFF_MISC);
 
   const int warp = threadIdx.x >> 5;
@@ -347,7 +356,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     mbar_init(BAR_Q_EMPTY, 1);
     for (int s = 0; s < C::NSLOT; ++s) {
       mbar_init(BAR_KV_FULL + 8 * s, 1);
-      mbar_init(BAR_KV_EMPTY + 8 * s, 1);
+      // FP8: V tiles (odd slots) are released by the two widening warps
+      mbar_init(BAR_KV_EMPTY + 8 * s, (FP8 && (s & 1)) ? 2 : 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(BAR_S_FULL + 8 * t, 1);
@@ -358,6 +368,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_init(BAR_O_FULL + 8 * t, 1);
     }
     mbar_init(BAR_DRAIN, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(BAR_VF_FULL + 8 * b, 2);   // one elected arrive per widening warp
+      mbar_init(BAR_VF_EMPTY + 8 * b, 1);  // the MMA thread's commit
+    }
     ctl->abort_flag = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
@@ -441,9 +455,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         issue_qk<D, FP8, F16>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
                          kv_smem + slot * C::KV_TILE_BYTES);
       };
-      auto issue_o = [&](int t, uint32_t slot, int half, bool acc) {
-        issue_pv_half<D, FP8, F16>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN,
-                              kv_smem + slot * C::KV_TILE_BYTES, half, acc);
+      // V operand of O += P V: the staged tile, or (FP8) its widened copy
+      auto issue_o = [&](int t, uint32_t v_smem, int half, bool acc) {
+        issue_pv_half<D, FP8, F16>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN, v_smem,
+                                   half, acc);
       };
 
       for (int i = 0; ok; ++i) {
@@ -470,7 +485,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
           const uint32_t itk = itv + 1, kslot = itk % C::NSLOT;
           const bool more = j + 1 < U.nmax;
-          if (!wait_bounded(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+          // FP8: the widening warps wait for the staged V tile; this thread
+          // waits for their fp16 copy (buffer = V use parity)
+          const uint32_t vuse = itv >> 1, vbuf = vuse & 1u;
+          const uint32_t v_smem = FP8 ? sbase + C::OFF_VF + vbuf * C::V16_TILE_BYTES
+                                      : kv_smem + vslot * C::KV_TILE_BYTES;
+          if (FP8) {
+            if (!wait_bounded(BAR_VF_FULL + 8 * vbuf, (vuse >> 1) & 1u, ctl, P)) { ok = false; break; }
+          } else {
+            if (!wait_bounded(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+          }
           tc_fence_after();
 #pragma unroll
           for (int t = 0; t < 2; ++t) {
@@ -479,7 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               for (int h = 0; ok && h < 2; ++h) {
                 if (!wait_bounded(BAR_P_FULL + 16 * t + 8 * h, pc[t] & 1u, ctl, P)) { ok = false; break; }
                 tc_fence_after();
-                issue_o(t, vslot, h, j > 0);
+                issue_o(t, v_smem, h, j > 0);
               }
               if (!ok) break;
               ++pc[t];
@@ -495,7 +519,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (!ok) break;
-          tc_commit(BAR_KV_EMPTY + 8 * vslot);
+          tc_commit(FP8 ? BAR_VF_EMPTY + 8 * vbuf : BAR_KV_EMPTY + 8 * vslot);
           if (more) {
             tc_commit(BAR_KV_EMPTY + 8 * kslot);
             if (j + 2 == U.nmax) tc_commit(BAR_Q_EMPTY);
@@ -509,6 +533,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       drain_wait(BAR_DRAIN, 0u, P);
     }
     __syncwarp();
+  } else if (FP8 && warp >= WARP_WIDEN) {
+    // ------------------------------------------------ V widening (FP8 only)
+    // Each staged E4M3 V tile is copied to fp16 (exactly) in one of two
+    // buffers, so that O += P V can keep P in fp16; the staged slot is then
+    // released here. Same units and fill order as the producer.
+    const int wtid = threadIdx.x - WARP_WIDEN * 32;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int i = 0; ok; ++i) {
+      Unit U;
+      const int st = cta_unit(i, P, U);
+      if (st == 0) break;
+      if (st == 1 || U.nmax == 0) continue;
+      for (int j = 0; j < U.nmax; ++j) {
+        const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
+        const uint32_t vuse = itv >> 1, vbuf = vuse & 1u;
+        bool w = wait_bounded(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u, ctl, P);
+        w = w && wait_bounded(BAR_VF_EMPTY + 8 * vbuf, ((vuse >> 1) & 1u) ^ 1u, ctl, P);
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        widen_v_tile<D>(sbase + C::OFF_KV + vslot * C::KV_TILE_BYTES,
+                        sbase + C::OFF_VF + vbuf * C::V16_TILE_BYTES, wtid, 64);
+        fence_proxy_async_smem();  // the fp16 tile is read by the tensor cores
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(BAR_VF_FULL + 8 * vbuf);
+          mbar_arrive(BAR_KV_EMPTY + 8 * vslot);
+        }
+      }
+      it += 2 * U.nmax;
+    }
   } else {
     // ------------------------------------------------------------- softmax
     const int t = warp >> 2;           // Q tile handled by this warpgroup
@@ -591,20 +645,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // per-column-half exponent scales. FP8: the first and second 64 keys
         // of the tile are two scale blocks of K and of V; e_* = log2 of the
         // factor p is multiplied by before rounding to E4M3, inv_* = 1 / that
-        // factor (2^-P_SCALE_LOG2 * largest V scale / V block scale).
+        // factor (largest V scale / V block scale).
         float c_lo = cq, c_hi = cq;
-        float e_lo = P_SCALE_LOG2, e_hi = P_SCALE_LOG2;
-        float inv_lo = 1.f / (1 << static_cast<int>(P_SCALE_LOG2)), inv_hi = inv_lo;
+        float e_lo = 0.f, e_hi = 0.f;
+        float inv_lo = 1.f, inv_hi = 1.f;
         if (FP8 && ks_row != nullptr) {
           const int kb0 = 2 * (U.j0 + j), kb1 = kb0 + 1;
           const float vs0 = vs_row[kb0];
           const float vs1 = kb1 < nblk_k ? vs_row[kb1] : v_ref;
           c_lo = cq * ks_row[kb0];
           c_hi = cq * (kb1 < nblk_k ? ks_row[kb1] : 1.f);
-          e_lo = P_SCALE_LOG2 + __log2f(vs0 / v_ref);
-          e_hi = P_SCALE_LOG2 + __log2f(vs1 / v_ref);
-          inv_lo = v_ref / (vs0 * (1 << static_cast<int>(P_SCALE_LOG2)));
-          inv_hi = v_ref / (vs1 * (1 << static_cast<int>(P_SCALE_LOG2)));
+          e_lo = __log2f(vs0 / v_ref);
+          e_hi = __log2f(vs1 / v_ref);
+          inv_lo = v_ref / vs0;
+          inv_hi = v_ref / vs1;
         }
         // row max of each 64-key half (raw scores; the exponent scale of a
         // half is positive, so it commutes with the max)
@@ -640,9 +694,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const bool rescale_o = j > 0 && __any_sync(0xffffffffu, need);
 
         // p = 2^(s * c - m): paired fp32 FMA, one MUFU ex2 per key, paired
-        // sums. FP8: p' = p * rr * 2^P_SCALE_LOG2 with log2(rr * 2^P_SCALE_LOG2)
-        // folded into the offset; each half sums its p' separately and is
-        // divided back when added to l.
+        // sums. FP8: p' = p * rr, rr = V block scale / v_ref (log2 rr folded
+        // into the offset) so that P V runs on the V codes; each half sums
+        // its p' separately and is divided back when added to l. P is kept
+        // in fp16 for FP8 and fp16 inputs, bf16 otherwise.
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
           const float cc = i ? c_hi : c_lo;
@@ -650,7 +705,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint64_t cc2 = f2_pack(cc, cc), off2 = f2_pack(off, off);
           uint64_t acc0 = 0ull, acc1 = 0ull;  // (+0, +0) pairs
           const float* h = s + 64 * i;
-          if constexpr (!FP8) {
+          {
             uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
@@ -661,25 +716,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
               acc0 = f2_add(acc0, f2_pack(p0, p1));
               acc1 = f2_add(acc1, f2_pack(p2, p3));
-              pk[c] = F16 ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
-              pk[c + 1] = F16 ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
+              pk[c] = (F16 || FP8) ? pack_f16x2(p0, p1) : pack_bf16x2(p0, p1);
+              pk[c + 1] = (F16 || FP8) ? pack_f16x2(p2, p3) : pack_bf16x2(p2, p3);
             }
             tmem_st32(t_lane + col_s + 32 * i, pk);
-          } else {
-            uint32_t phi[16], plo[16];
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              float x0, x1, x2, x3;
-              f2_unpack(f2_fma(f2_pack(h[4 * c], h[4 * c + 1]), cc2, off2), x0, x1);
-              f2_unpack(f2_fma(f2_pack(h[4 * c + 2], h[4 * c + 3]), cc2, off2), x2, x3);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              const float p2 = ex2_approx(x2), p3 = ex2_approx(x3);
-              acc0 = f2_add(acc0, f2_pack(p0, p1));
-              acc1 = f2_add(acc1, f2_pack(p2, p3));
-              split_e4m3x4(p0, p1, p2, p3, phi[c], plo[c]);
-            }
-            tmem_st16(t_lane + col_s + 16 * i, phi);
-            tmem_st16(t_lane + col_s + C::P_COLS + 16 * i, plo);
           }
           float q0, q1, q2, q3;
           f2_unpack(acc0, q0, q1);
@@ -718,8 +758,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++oc;
           if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
           tc_fence_after();
-          inv = l_run > 0.f ? v_ref / (FP8 ? l_run * (1 << static_cast<int>(P_SCALE_LOG2)) : l_run)
-                            : 0.f;
+          inv = l_run > 0.f ? v_ref / l_run : 0.f;
 #pragma unroll
           for (int i = 0; i < D / 32; ++i) {
             uint32_t r[32];
@@ -748,10 +787,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++oc;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
-        // FP8: O holds sum p * 2^P_SCALE_LOG2 * (V block scale / v_ref) * code
-        const float inv =
-            l_run > 0.f ? v_ref / (FP8 ? l_run * (1 << static_cast<int>(P_SCALE_LOG2)) : l_run)
-                        : 0.f;
+        // FP8: O holds sum p * (V block scale / v_ref) * code
+        const float inv = l_run > 0.f ? v_ref / l_run : 0.f;
 #pragma unroll
         for (int i = 0; i < D / 32; ++i) {
           uint32_t r[32];

@@ -82,28 +82,6 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a0, float a1, float a2, fl
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-// Four non-negative fp32 -> two E4M3 quads (hi, lo) with hi + lo close to the
-// inputs: the pair is first rounded to f16, hi is the E4M3 rounding of that,
-// and lo the E4M3 rounding of the (exact, in f16) remainder. hi alone keeps 4
-// significant bits; hi + lo about 8. Element 0 goes to bits 0..7.
-__device__ __forceinline__ void split_e4m3x4(float a0, float a1, float a2, float a3,
-                                             uint32_t& hi, uint32_t& lo) {
-  uint32_t p01, p23, h01, h23, r01, r23;
-  unsigned short hq01, hq23, lq01, lq23;
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p01) : "f"(a1), "f"(a0));
-  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(p23) : "f"(a3), "f"(a2));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hq01) : "r"(p01));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(hq23) : "r"(p23));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h01) : "h"(hq01));
-  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h23) : "h"(hq23));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r01) : "r"(p01), "r"(h01));
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r23) : "r"(p23), "r"(h23));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lq01) : "r"(r01));
-  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(lq23) : "r"(r23));
-  hi = static_cast<uint32_t>(hq01) | (static_cast<uint32_t>(hq23) << 16);
-  lo = static_cast<uint32_t>(lq01) | (static_cast<uint32_t>(lq23) << 16);
-}
-
 // -------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -323,6 +301,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory writes visible to the
+// async proxy (TMA, tcgen05.mma operand reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void sts128(uint32_t addr, const uint4& v) {
+  asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Two E4M3 codes (low byte first) -> packed f16x2, exact (every E4M3 value is
+// an fp16 value).
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<unsigned short>(two_codes)));
+  return r;
 }
 
 }  // namespace attnb3

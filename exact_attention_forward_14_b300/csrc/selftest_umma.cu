@@ -9,9 +9,9 @@
 //   form 1 ("PV"): D[128 x d]   = A[128 x 128] * B[128 x d], A written to
 //                  tensor memory by the threads (the P operand), B staged by
 //                  TMA with d contiguous (the O += P V step). For E4M3, A is
-//                  given as two parts (128 x 256 bytes: hi codes, then lo
-//                  codes, per row) and D = (hi + lo) * B, as the kernel's
-//                  split P is consumed.
+//                  fp16 (as the kernel keeps P) and B is staged as E4M3 codes
+//                  and widened to fp16 in shared memory first, as the kernel
+//                  does.
 // d = 128; element type bf16 or E4M3. D is returned as fp32 row-major.
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -50,10 +50,11 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t a_smem = sbase;                    // Q-tile sized region
   const uint32_t b_smem = sbase + C::Q_TILE_BYTES;  // K/V-tile sized region
-  const uint32_t bar_load = b_smem + C::KV_TILE_BYTES;
+  const uint32_t vf_smem = sbase + 64 * 1024;       // E4M3 PV form: widened V
+  const uint32_t bar_load = sbase + 96 * 1024;
   const uint32_t bar_mma = bar_load + 8;
-  volatile uint32_t* tmem_holder = reinterpret_cast<volatile uint32_t*>(
-      smem + C::Q_TILE_BYTES + C::KV_TILE_BYTES + 16);
+  volatile uint32_t* tmem_holder =
+      reinterpret_cast<volatile uint32_t*>(smem + 96 * 1024 + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
@@ -87,14 +88,16 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         tmem_st32(t_lane + 128 + 32 * i, pk);
       }
     } else {
-      // two parts (hi, lo) of 128 E4M3 codes each; the MMA sums both
-      const uint32_t* ar = reinterpret_cast<const uint32_t*>(a_raw + row * 256);
+      // fp16 P (the FP8 path keeps P in fp16): raw bits, packed like bf16
+      const uint16_t* ar = reinterpret_cast<const uint16_t*>(a_raw) + row * 128;
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
+      for (int h = 0; h < 2; ++h) {
         uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = ar[32 * part + c];  // first key in bits 0..7
-        tmem_st32(t_lane + 128 + C::P_COLS * part, pk);
+        for (int c = 0; c < 32; ++c)
+          pk[c] = static_cast<uint32_t>(ar[64 * h + 2 * c]) |
+                  (static_cast<uint32_t>(ar[64 * h + 2 * c + 1]) << 16);
+        tmem_st32(t_lane + 128 + 32 * h, pk);
       }
     }
     tmem_st_wait();
@@ -113,16 +116,24 @@ __global__ void __launch_bounds__(ST_THREADS, 1)
         tma_load_4d(a_smem + c * C::Q_CHUNK_BYTES, &tm_a, bar_load, c * C::CHUNK_ELEMS, 0, 0, 0);
       tma_load_4d(b_smem + c * C::KV_CHUNK_BYTES, &tm_b, bar_load, c * C::CHUNK_ELEMS, 0, 0, 0);
     }
-    ok = st_wait(bar_load, 0);
+  }
+  // every thread: the staged tiles have landed (FP8 PV form: widen V to fp16)
+  const bool landed = st_wait(bar_load, 0);
+  if (FP8 && FORM == 1 && landed) {
+    widen_v_tile<D>(b_smem, vf_smem, threadIdx.x, ST_THREADS);
+    fence_proxy_async_smem();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    ok = landed;
     if (ok) {
       tc_fence_after();
       if (FORM == 0) issue_qk<D, FP8>(tmem, a_smem, b_smem);
-      else issue_pv<D, FP8>(tmem, tmem + 128, b_smem, false);
+      else issue_pv<D, FP8>(tmem, tmem + 128, FP8 ? vf_smem : b_smem, false);
       tc_commit(bar_mma);
       ok = st_wait(bar_mma, 0);
     }
     if (!ok) atomicExch(err, 1);
-    if (!ok) st_wait(bar_load, 0);  // let the copy land before exit
   }
   tc_fence_before();
   __syncthreads();
@@ -167,7 +178,7 @@ int run_selftest(const void* a, const void* b, float* out, int* err, cudaStream_
 extern "C" {
 
 // form: 0 = QK form, 1 = PV form; fp8: 0 = bf16, 1 = E4M3. a, b: device,
-// 128 x 128 row-major (a: 128 x 256 bytes for the E4M3 PV form); out: device
+// 128 x 128 row-major (a: fp16 bits for the E4M3 PV form); out: device
 // fp32 128 x 128; err: device int set to 1 if a wait timed out. Returns an
 // attn_status_t.
 int attn_selftest_umma(int form, int fp8, const void* a, const void* b, float* out, int* err,

@@ -1,6 +1,7 @@
 """Single-tile checks of the two tcgen05 contraction forms the kernel uses
 (S = Q K^T with both operands K-major in shared memory; O = P V with P in
-tensor memory and V d-contiguous; for E4M3, P in two parts), against torch
+tensor memory and V d-contiguous; for E4M3 inputs, P in fp16 and the E4M3 V
+tile widened to fp16 in shared memory as the kernel does), against torch
 matmul in fp32."""
 import ctypes
 import os
@@ -31,12 +32,14 @@ def _single_tile(form, fp8):
         b = b32.to(torch.bfloat16)
     af, bf = a.float(), b.float()
     if fp8 and form == 1:
-        # the P operand in two E4M3 parts: hi codes, then the codes of the remainder
-        lo = (a32 - af).to(torch.float8_e4m3fn)
-        af = af + lo.float()
-        a = torch.cat([a.view(torch.uint8), lo.view(torch.uint8)], dim=1).contiguous()
+        # the FP8 path keeps P in fp16 and widens the E4M3 V tile to fp16
+        a = a32.to(torch.float16)
+        af = a.float()
     ref = af @ bf.T if form == 0 else af @ bf
-    da = a.view(torch.uint8).cuda() if fp8 else a.cuda()
+    if fp8 and form == 1:
+        da = a.cuda()
+    else:
+        da = a.view(torch.uint8).cuda() if fp8 else a.cuda()
     db = b.view(torch.uint8).cuda() if fp8 else b.cuda()
     out = torch.full((128, 128), float("nan"), device="cuda")
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
