@@ -227,11 +227,13 @@ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; 
 // L2, not HBM. With split-KV, item w covers key range w % nsplit of pair
 // w / nsplit.
 //
-// Longest-first order (lpt != 0; chosen by the host when there are fewer
-// than 4 items per CTA, where whole items leave the last round part-empty):
-// single units sorted by level, highest (most K/V tiles) first, dealt to the
-// CTAs in a snake (round r goes left to right for even r, right to left for
-// odd r), which evens out the per-CTA totals.
+// Single-unit order (lpt != 0; chosen by the host when there are fewer than
+// 4 items per CTA, where whole items leave the last round part-empty): single
+// units dealt to the CTAs in a snake (round r goes left to right for even r,
+// right to left for odd r), which evens out the per-CTA totals. Under a
+// causal mask the units are sorted by level, highest (most K/V tiles) first,
+// across all heads; without one every unit costs the same and they stay
+// head-major, so the few heads in flight keep their K/V in L2.
 
 // Fills U for unit (level, bh, split); the key range is split's K/V tiles.
 __device__ __forceinline__ void fill_unit(int level, int bh, int split, const FwdParams& P,
@@ -269,7 +271,10 @@ __device__ __forceinline__ int cta_unit(int i, const FwdParams& P, Unit& U) {
     const int kg = i * G + ((i & 1) ? G - 1 - c : c);
     const int bh_count = P.B * P.Hq;
     if (kg >= bh_count * P.n_qp) return 0;
-    fill_unit(P.n_qp - 1 - kg / bh_count, kg % bh_count, 0, P, U);
+    if (P.causal)  // costs differ by level: highest level first, all heads
+      fill_unit(P.n_qp - 1 - kg / bh_count, kg % bh_count, 0, P, U);
+    else           // equal costs: keep heads together (their K/V stay in L2)
+      fill_unit(kg % P.n_qp, kg / P.n_qp, 0, P, U);
     return 2;
   }
   int w = c + (i >> 1) * G;
