@@ -58,7 +58,8 @@ def _fp8_case(oracle_mod, torch, q, k, v, causal, scale, rows=None):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("shape", [(1, 2, 2, 128, 128, 128, False), (2, 4, 2, 300, 300, 128, True),
-                                   (1, 2, 2, 200, 517, 128, False), (1, 4, 4, 513, 513, 64, True)])
+                                   (1, 2, 2, 200, 517, 128, False), (1, 4, 4, 513, 513, 64, True),
+                                   (1, 8, 2, 700, 1100, 128, True), (2, 4, 1, 900, 333, 64, True)])
 def test_fp8_attention_small(oracle_mod, shape):
     torch = require_gpu()
     B, Hq, Hkv, Sq, Sk, d, causal = shape

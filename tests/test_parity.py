@@ -167,3 +167,29 @@ def test_f16_full_size_sampled_rows(oracle_mod):
     o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
     assert_o_close(o_g, o_ref, kind="f16")
     assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref)
+
+
+# ------------------------------------------------------------- large sizes --
+
+@pytest.mark.gpu
+def test_long_sequence_near_the_index_limit(oracle_mod):
+    """Sq = Sk = 131072 with 16 heads: 268M elements per tensor (the 32-bit
+    element-count guard allows up to 2^31 - 1), K/V tile coordinates up to
+    1024 tiles, causal; sampled rows across the whole range against the
+    oracle, including the first and the last row."""
+    torch = require_gpu()
+    B, H, S, d = 1, 16, 131072, 128
+    g = torch.Generator().manual_seed(77)
+    q = torch.randn(B, S, H, d, generator=g).to(torch.bfloat16)
+    k = torch.randn(B, S, H, d, generator=g).to(torch.bfloat16)
+    v = torch.randn(B, S, H, d, generator=g).to(torch.bfloat16)
+    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=True)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    rows = inputs.sample_rows(B, H, S, 120, seed=7)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
+                                         True, 1.0 / np.sqrt(d), rows=rows)
+    b, rem = np.divmod(rows, H * S)
+    h, i = np.divmod(rem, S)
+    o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
+    assert_o_close(o_g, o_ref)
+    assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref)
