@@ -59,6 +59,9 @@ def _load():
         lib.oracle_rmsnorm_heads.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                              ctypes.c_void_p, ctypes.c_longlong, ctypes.c_int,
                                              ctypes.c_int, ctypes.c_double]
+        lib.oracle_attn_bwd.restype = ctypes.c_int
+        lib.oracle_attn_bwd.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 3
+                                        + [ctypes.c_int] * 7 + [ctypes.c_double])
         lib.oracle_attn_fwd.restype = ctypes.c_int
         lib.oracle_attn_fwd.argtypes = (
             [ctypes.c_void_p] * 6 + [ctypes.c_int] + [ctypes.c_void_p] * 2
@@ -173,3 +176,24 @@ def attn_fwd(q, k, v, causal: bool, scale: float, dtype: str = "bf16",
     if rc != 0:
         raise ValueError("oracle rejected the dimensions")
     return o, lse
+
+
+def attn_bwd(q, k, v, d_o, causal: bool, scale: float, dtype: str = "bf16"):
+    """fp64 gradients (dq, dk, dv) of sum(d_o * O) for O = attn_fwd(q, k, v);
+    q, d_o: [B, Sq, Hq, d], k, v: [B, Sk, Hkv, d], 16-bit bits (bf16 or f16)."""
+    lib = _load()
+    if dtype not in ("bf16", "f16"):
+        raise ValueError(f"unknown dtype {dtype!r}")
+    q, k, v, d_o = (np.ascontiguousarray(x).view(np.uint16) for x in (q, k, v, d_o))
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    dq = np.empty(q.shape, dtype=np.float64)
+    dk = np.empty(k.shape, dtype=np.float64)
+    dv = np.empty(v.shape, dtype=np.float64)
+    rc = lib.oracle_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(d_o),
+                             DTYPE_F16 if dtype == "f16" else DTYPE_BF16,
+                             _ptr(dq), _ptr(dk), _ptr(dv), B, Hq, Hkv, Sq, Sk, d,
+                             int(bool(causal)), float(scale))
+    if rc != 0:
+        raise ValueError("oracle rejected the dimensions")
+    return dq, dk, dv

@@ -47,6 +47,16 @@
  * division and the amax are evaluated in fp32, the precision in which the
  * quantised code is decided.
  *
+ * Backward (oracle_attn_bwd): the pages give no backward algorithm; the
+ * gradients of sum(dO * O) are the chain rule through the definition above,
+ * written out in fp64 per (query row, visible key) pair:
+ *   P_ij = exp(s_ij - LSE_i),  dP_ij = dO_i . v_j,  D_i = dO_i . O_i,
+ *   dS_ij = P_ij (dP_ij - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_i dS_ij q_i,
+ *   dV_j = sum_i P_ij dO_i,
+ * GQA query heads summing into their KV head; rows with no visible key get
+ * dQ = 0 and contribute nothing.
+ *
  * Build: gcc -O2 -fopenmp -shared -fPIC attn_oracle.c -o liboracle.so -lm
  */
 #include <math.h>
@@ -253,6 +263,78 @@ static double attn_row(const oracle_inputs* in, int causal, double scale, int b,
     }
     for (int c = 0; c < d; ++c) o_row[c] = acc[c] / l;
     return m + log(l);
+}
+
+static int check_dims_bwd(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || d <= 0) return 1;
+    return Hq % Hkv != 0;
+}
+
+/* ------------------------------------------------------------- backward -- */
+
+/* Gradient of the loss L = sum(dO * O) through O = softmax(scale Q K^T + mask) V
+ * (the pages give no backward algorithm; this is the chain rule written out):
+ *   P_ij  = exp(s_ij - LSE_i)                          (visible j, else 0)
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . V_j
+ *   D_i   = sum_j P_ij dP_ij  (= dO_i . O_i)
+ *   dS_ij = P_ij (dP_ij - D_i)
+ *   dQ_i  = scale sum_j dS_ij K_j,   dK_j = scale sum_i dS_ij Q_i
+ * with GQA query heads summed into their KV head's dK and dV. Inputs as for
+ * oracle_attn_fwd (16-bit bits: bf16 or fp16), dO with O's shape; outputs fp64:
+ * dq [B,Sq,Hq,d], dk / dv [B,Sk,Hkv,d]. Recomputes LSE itself in fp64. */
+int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* d_o, int dtype,
+                    double* dq, double* dk, double* dv,
+                    int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal, double scale) {
+    if (check_dims_bwd(B, Hq, Hkv, Sq, Sk, d)) return 1;
+    if (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_F16) return 1;
+    oracle_inputs in = {q, k, v, NULL, NULL, NULL, dtype, B, Hq, Hkv, Sq, Sk, d};
+    oracle_inputs gin = {d_o, NULL, NULL, NULL, NULL, NULL, dtype, B, Hq, Hkv, Sq, Sk, d};
+    const int group = Hq / Hkv;
+    memset(dk, 0, sizeof(double) * (size_t)B * Sk * Hkv * d);
+    memset(dv, 0, sizeof(double) * (size_t)B * Sk * Hkv * d);
+    /* one (b, hkv) per task: its query heads' contributions go to its dk / dv */
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+    for (int b = 0; b < B; ++b)
+        for (int hk = 0; hk < Hkv; ++hk) {
+            double* o_row = (double*)malloc(sizeof(double) * 2 * (size_t)d);
+            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+            double* dorow = o_row + d;
+            for (int hq = hk * group; hq < (hk + 1) * group; ++hq)
+                for (int i = 0; i < Sq; ++i) {
+                    double lse = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+                    double* dqrow = dq + (((size_t)b * Sq + i) * Hq + hq) * (size_t)d;
+                    for (int c = 0; c < d; ++c) {
+                        dqrow[c] = 0.0;
+                        dorow[c] = load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c);
+                    }
+                    if (lse == -INFINITY) continue; /* no visible key: zero gradient */
+                    long jmax = Sk - 1;
+                    if (causal && (long)i + Sk - Sq < jmax) jmax = (long)i + Sk - Sq;
+                    double D = 0.0;
+                    for (int c = 0; c < d; ++c) D += dorow[c] * o_row[c];
+                    for (long j = 0; j <= jmax; ++j) {
+                        double dot = 0.0, dp = 0.0;
+                        for (int c = 0; c < d; ++c) {
+                            double qv = load_elem(&in, q, NULL, Sq, Hq, b, i, hq, c);
+                            dot += qv * load_elem(&in, k, NULL, Sk, Hkv, b, (int)j, hk, c);
+                            dp += dorow[c] * load_elem(&in, v, NULL, Sk, Hkv, b, (int)j, hk, c);
+                        }
+                        const double p = exp(scale * dot - lse);
+                        const double ds = p * (dp - D);
+                        double* dkrow = dk + (((size_t)b * Sk + j) * Hkv + hk) * (size_t)d;
+                        double* dvrow = dv + (((size_t)b * Sk + j) * Hkv + hk) * (size_t)d;
+                        for (int c = 0; c < d; ++c) {
+                            dqrow[c] += scale * ds * load_elem(&in, k, NULL, Sk, Hkv, b, (int)j, hk, c);
+                            dkrow[c] += scale * ds * load_elem(&in, q, NULL, Sq, Hq, b, i, hq, c);
+                            dvrow[c] += p * dorow[c];
+                        }
+                    }
+                }
+            free(o_row);
+            free(work);
+        }
+    return 0;
 }
 
 static int check_dims(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
