@@ -1,11 +1,13 @@
-"""Exact attention forward for B300 (sm_103a): Python binding of libattn_b300.
+"""Exact attention for B300 (sm_103a): Python binding of libattn_b300.
 
 The functions named like the C ABI (``attn_fwd``, ``attn_fwd_fp8``,
-``attn_quantize_fp8_e4m3``, ``attn_device_status``, ``attn_status_string``)
-only marshal arguments: tensors become device pointers, a torch stream (or
-None = torch's current stream) becomes a cudaStream_t; they return the C
-status code. ``forward``, ``forward_fp8`` and ``quantize_fp8`` additionally
-allocate the outputs with torch and raise ``AttnError`` on a non-zero status.
+``attn_fwd_splitkv``, ``attn_bwd``, ``attn_quantize_fp8_e4m3``,
+``attn_device_status``, ``attn_status_string``, ...) only marshal arguments:
+tensors become device pointers, a torch stream (or None = torch's current
+stream) becomes a cudaStream_t; they return the C status code. ``forward``,
+``forward_fp8``, ``forward_splitkv``, ``backward`` and ``quantize_fp8``
+additionally allocate the outputs with torch and raise ``AttnError`` on a
+non-zero status.
 All compute runs in the CUDA library; there is no fallback path: if the
 library is missing every call raises.
 """
@@ -20,7 +22,8 @@ __all__ = [
     "ATTN_OK", "ATTN_ERR_INVALID_ARG", "ATTN_ERR_UNSUPPORTED", "ATTN_ERR_MISALIGNED",
     "ATTN_ERR_CUDA", "ATTN_ERR_TIMEOUT", "ATTN_BF16", "ATTN_FP8_E4M3", "ATTN_F16", "AttnError",
     "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc",
-    "attn_splitkv_plan", "attn_qk_rmsnorm", "qk_rmsnorm",
+    "attn_splitkv_plan", "attn_qk_rmsnorm", "qk_rmsnorm", "attn_bwd", "attn_bwd_workspace_size",
+    "backward",
     "attn_quantize_fp8_e4m3", "attn_device_status",
     "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
     "library_path", "load",
@@ -82,6 +85,11 @@ def load():
         lib.attn_qk_rmsnorm.restype = I
         lib.attn_quantize_fp8_e4m3.argtypes = [P, P, P, I, I, I, I, P]
         lib.attn_quantize_fp8_e4m3.restype = I
+        lib.attn_bwd.argtypes = [P, P, P, P, P, P, P, P, P, I, I, I, I, I, I, I, F, I, P,
+                                 ctypes.c_size_t, P]
+        lib.attn_bwd.restype = I
+        lib.attn_bwd_workspace_size.argtypes = [I, I, I, ctypes.POINTER(ctypes.c_size_t)]
+        lib.attn_bwd_workspace_size.restype = I
         lib.attn_device_status.argtypes = [P]
         lib.attn_device_status.restype = I
         lib.attn_status_string.argtypes = [I]
@@ -162,6 +170,21 @@ def attn_qk_rmsnorm(q, k, q_weight, k_weight, q_out, k_out, B, Sq, Sk, Hq, Hkv, 
 def attn_quantize_fp8_e4m3(x, codes, scale, B, S, H, d, stream=None) -> int:
     return load().attn_quantize_fp8_e4m3(_ptr(x), _ptr(codes), _ptr(scale), int(B), int(S),
                                          int(H), int(d), _stream(stream))
+
+
+def attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, dtype,
+             workspace, workspace_bytes, stream=None) -> int:
+    return load().attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(d_o), _ptr(dq),
+                           _ptr(dk), _ptr(dv), int(B), int(Hq), int(Hkv), int(Sq), int(Sk),
+                           int(d), int(bool(causal)), float(scale), int(dtype), _ptr(workspace),
+                           int(workspace_bytes), _stream(stream))
+
+
+def attn_bwd_workspace_size(B, Hq, Sq):
+    """Returns (status, workspace_bytes)."""
+    w = ctypes.c_size_t(0)
+    rc = load().attn_bwd_workspace_size(int(B), int(Hq), int(Sq), ctypes.byref(w))
+    return rc, w.value
 
 
 def attn_device_status(stream=None) -> int:
@@ -251,6 +274,31 @@ def forward_splitkv(q, k, v, causal: bool = False, scale: float | None = None,
                             num_splits, workspace, workspace.numel() * workspace.element_size(),
                             stream), "attn_fwd_splitkv")
     return out, lse
+
+
+def backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = None,
+             workspace=None, out=None, stream=None):
+    """Gradients (dq, dk, dv) of sum(d_o * O) for the forward pass that gave
+    (o, lse) on (q, k, v); bf16 or fp16, CUDA, contiguous. The fp32 workspace
+    is allocated with torch unless given; out = (dq, dk, dv) or None."""
+    import torch
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    code = ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    rc, need = attn_bwd_workspace_size(B, Hq, Sq)
+    _check(rc, "attn_bwd_workspace_size")
+    if workspace is None:
+        workspace = torch.empty(need // 4, dtype=torch.float32, device=q.device)
+    dq, dk, dv = out if out is not None else (torch.empty_like(q), torch.empty_like(k),
+                                              torch.empty_like(v))
+    for t in (q, k, v, o, lse, d_o, dq, dk, dv):
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+    _check(attn_bwd(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, d, causal, scale, code,
+                    workspace, workspace.numel() * workspace.element_size(), stream), "attn_bwd")
+    return dq, dk, dv
 
 
 def qk_rmsnorm(q, k, q_weight, k_weight, eps: float = 1e-6, out=None, stream=None):

@@ -1,6 +1,7 @@
 // attn_api.cu -- host side of libattn_b300.so: argument validation, TMA
-// tensor-map encoding, launch of the fused attention kernel and of the FP8
-// block quantiser, and the device status word.
+// tensor-map encoding, launch of the fused attention kernels (forward,
+// split-KV merge, backward), the QK-RMSNorm prologue and the FP8 block
+// quantiser, and the device status word.
 //
 // The C ABI is declared (with argument meaning, layouts, ownership and error
 // behaviour) in include/attn_b300.h.
@@ -14,6 +15,7 @@
 #include <mutex>
 
 #include "attn_b300.h"
+#include "attn_bwd_kernel.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "quantize_fp8.cuh"
 #include "qk_rmsnorm.cuh"
@@ -220,6 +222,83 @@ int launch_combine(const float* o_part, const float* lse_part, void* o, float* l
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+// ---- backward pass ---------------------------------------------------------
+
+size_t bwd_sq_pad(int Sq) {
+  return (static_cast<size_t>(Sq) + attnb3::BWD_TILE - 1) / attnb3::BWD_TILE * attnb3::BWD_TILE;
+}
+
+size_t bwd_workspace_bytes(int B, int Hq, int Sq) {
+  return 2 * static_cast<size_t>(B) * Hq * bwd_sq_pad(Sq) * sizeof(float);
+}
+
+template <int D, bool F16>
+int launch_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+               const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+               int Sk, int causal, float scale, float* ws, cudaStream_t stream, DeviceInfo* di,
+               uint32_t attr_bit) {
+  using C = attnb3::BwdCfg<D, F16>;
+  auto kkv = attnb3::bwd_dkdv_kernel<D, F16>;
+  auto kq = attnb3::bwd_dq_kernel<D, F16>;
+  if (!(di->attr_done.load(std::memory_order_acquire) & attr_bit)) {
+    if (cudaFuncSetAttribute(kkv, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(kq, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+            cudaSuccess)
+      return ATTN_ERR_CUDA;
+    di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
+  }
+  CUtensorMap tq, tdo, tk, tv, tk64, tv64;
+  if (!encode_bshd(&tq, q, false, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
+      !encode_bshd(&tdo, d_o, false, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
+      !encode_bshd(&tk, k, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
+      !encode_bshd(&tv, v, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
+      !encode_bshd(&tk64, k, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_KV_ROWS, F16) ||
+      !encode_bshd(&tv64, v, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_KV_ROWS, F16))
+    return ATTN_ERR_CUDA;
+
+  const size_t sq_pad = bwd_sq_pad(Sq);
+  const long long rows_pad = static_cast<long long>(B) * Hq * static_cast<long long>(sq_pad);
+  attnb3::BwdParams P;
+  P.dq = static_cast<uint16_t*>(dq);
+  P.dk = static_cast<uint16_t*>(dk);
+  P.dv = static_cast<uint16_t*>(dv);
+  P.lse2 = ws;
+  P.dsum = ws + rows_pad;
+  P.B = B;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.Sq = Sq;
+  P.Sk = Sk;
+  P.Sq_pad = static_cast<int>(sq_pad);
+  P.group = Hq / Hkv;
+  P.causal = causal ? 1 : 0;
+  P.nq = static_cast<int>(sq_pad / attnb3::BWD_TILE);
+  P.nk = (Sk + attnb3::BWD_TILE - 1) / attnb3::BWD_TILE;
+  P.kv_npair = (P.nk + 1) / 2;
+  P.kv_items = B * Hkv * P.kv_npair;
+  P.n_qp = (Sq + attnb3::BWD_UNIT_ROWS - 1) / attnb3::BWD_UNIT_ROWS;
+  P.q_npair = (P.n_qp + 1) / 2;
+  P.q_items = B * Hq * P.q_npair;
+  P.nkv64 = (Sk + attnb3::BWD_KV_ROWS - 1) / attnb3::BWD_KV_ROWS;
+  P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  P.scale = scale;
+  P.timeout_ns = kWaitLimitNs;
+  P.status = di->status;
+
+  const long long per_block = attnb3::BWD_PREP_THREADS / 32;
+  const long long prep_blocks = (rows_pad + per_block - 1) / per_block;
+  attnb3::bwd_prep_kernel<D, F16><<<static_cast<unsigned>(prep_blocks),
+                                    attnb3::BWD_PREP_THREADS, 0, stream>>>(
+      static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, ws,
+      ws + rows_pad, Hq, Sq, P.Sq_pad, rows_pad);
+  const int gkv = P.kv_items < di->num_sms ? P.kv_items : di->num_sms;
+  kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
+  const int gq = P.q_items < di->num_sms ? P.q_items : di->num_sms;
+  kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk64, tv64, P);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
 // ---- workspace for attn_fwd_splitkv_noalloc --------------------------------
 // A fixed device array in this library, so that callers who may not allocate
 // device memory can still use the split-KV path. Every GPU that loads the
@@ -416,6 +495,49 @@ int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, 
                                 reinterpret_cast<cudaStream_t>(stream)>>>(x, codes, scale, S, H,
                                                                           d, nblk);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+int attn_bwd_workspace_size(int B, int Hq, int Sq, size_t* workspace_bytes) {
+  if (!workspace_bytes || B <= 0 || Hq <= 0 || Sq <= 0) return ATTN_ERR_INVALID_ARG;
+  *workspace_bytes = bwd_workspace_bytes(B, Hq, Sq);
+  return ATTN_OK;
+}
+
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+             int Sk, int d, int causal, float scale, int dtype, void* workspace,
+             size_t workspace_bytes, attn_stream_t stream) {
+  int rc = check_attn_args(q, k, v, const_cast<void*>(o), const_cast<float*>(lse), B, Hq, Hkv,
+                           Sq, Sk, d, scale);
+  if (rc != ATTN_OK) return rc;
+  if (!d_o || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+  // padded row statistics are indexed with 32-bit row counts
+  if (static_cast<long long>(B) * Hq * static_cast<long long>(bwd_sq_pad(Sq)) > 0x7fffffffLL)
+    return ATTN_ERR_INVALID_ARG;
+  if (!workspace || workspace_bytes < bwd_workspace_bytes(B, Hq, Sq))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(d_o, 16) || !aligned(dq, 16) || !aligned(dk, 16) || !aligned(dv, 16) ||
+      !aligned(workspace, 16))
+    return ATTN_ERR_MISALIGNED;
+  DeviceInfo* di = nullptr;
+  rc = current_device(&di);
+  if (rc != ATTN_OK) return rc;
+  if (!get_encoder()) return ATTN_ERR_CUDA;
+  const bool f16 = dtype == ATTN_F16;
+  float* ws = static_cast<float*>(workspace);
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 128 && !f16)
+    return launch_bwd<128, false>(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, causal,
+                                  scale, ws, st, di, 64u);
+  if (d == 64 && !f16)
+    return launch_bwd<64, false>(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, causal,
+                                 scale, ws, st, di, 128u);
+  if (d == 128)
+    return launch_bwd<128, true>(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, causal,
+                                 scale, ws, st, di, 256u);
+  return launch_bwd<64, true>(q, k, v, o, lse, d_o, dq, dk, dv, B, Hq, Hkv, Sq, Sk, causal,
+                              scale, ws, st, di, 512u);
 }
 
 int attn_device_status(attn_stream_t stream) {

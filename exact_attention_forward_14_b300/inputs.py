@@ -113,6 +113,14 @@ def draw_workload_16(w: Workload):
     return f(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
 
 
+def draw_grad_out(B, Sq, Hq, d, seed, dtype="bf16"):
+    """Upstream gradient dO [B, Sq, Hq, d] for the backward pass: fp32 N(0, 1)
+    from its own generator (seed + 500), rounded to the 16-bit type."""
+    g = torch.Generator().manual_seed(int(seed) + 500)
+    x = torch.randn((B, Sq, Hq, d), generator=g, dtype=torch.float32)
+    return x.to(torch.float16 if dtype == "f16" else torch.bfloat16)
+
+
 def draw_norm_weights(n, seed, dtype="bf16"):
     """RMSNorm weights ~ 1 + 0.25 N(0, 1), rounded to the 16-bit type."""
     g = torch.Generator().manual_seed(int(seed))

@@ -1,6 +1,7 @@
 /*
- * attn_b300.h -- C ABI of the B300 (sm_103a) exact attention forward library
- * (libattn_b300.so).
+ * attn_b300.h -- C ABI of the B300 (sm_103a) exact attention library
+ * (libattn_b300.so): forward pass, its split-KV and FP8 forms, the QK-RMSNorm
+ * prologue and the backward pass.
  *
  * The operation (FlashAttention-3 deep dive, techknowgenie.com/posts/
  * 109164421204410442, introduction and section "3-stage asynchronous software
@@ -204,6 +205,45 @@ int attn_qk_rmsnorm(const void* q, const void* k, const void* q_weight, const vo
  */
 int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale,
                            int B, int S, int H, int d, attn_stream_t stream);
+
+/*
+ * attn_bwd_workspace_size -- bytes of device workspace attn_bwd needs:
+ * 2 * B * Hq * Sq_pad * 4 with Sq_pad = Sq rounded up to a multiple of 128
+ * (one fp32 per padded query row for D = rowsum(dO * O) and one for
+ * LSE * log2(e)). Pure arithmetic. Returns an attn_status_t
+ * (ATTN_ERR_INVALID_ARG for a null output or non-positive sizes).
+ */
+int attn_bwd_workspace_size(int B, int Hq, int Sq, size_t* workspace_bytes);
+
+/*
+ * attn_bwd -- exact attention backward pass: the gradients of
+ * L = sum(d_o * O) for O = attn_fwd(q, k, v) with the same mask and scale.
+ * The pages define the forward pass only; these are its derivatives by the
+ * chain rule (no approximation), with P = exp(scale Q K^T - LSE):
+ *     dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D),
+ *     dQ = scale dS K,  dK = scale dS^T Q,
+ * the query heads sharing a KV head summing into its dK and dV, and rows with
+ * no visible key contributing nothing.
+ *   q, k, v    : the forward's inputs (layouts as attn_fwd)
+ *   o, lse     : the forward's outputs for them (lse in natural-log units)
+ *   d_o        : device input dL/dO, [B, Sq, Hq, d], q's element type
+ *   dq         : device output [B, Sq, Hq, d]
+ *   dk, dv     : device outputs [B, Sk, Hkv, d]
+ *   dtype      : ATTN_BF16 or ATTN_F16, for every 16-bit tensor here
+ *   workspace  : device buffer owned by the caller, 16-byte aligned, at least
+ *                attn_bwd_workspace_size bytes; contents on entry ignored, on
+ *                return undefined
+ * Other arguments as attn_fwd. P and dS are rounded to dtype before they
+ * enter the tensor cores (fp32 accumulation); the gradients are rounded to
+ * nearest in dtype. Three kernels are enqueued on `stream` (row statistics,
+ * dK/dV, dQ); every output element is written exactly once, so results are
+ * deterministic. Calls that share a workspace must not overlap. Errors as
+ * attn_fwd; ATTN_ERR_INVALID_ARG for a missing or too small workspace.
+ */
+int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
+             int Sk, int d, int causal, float scale, int dtype, void* workspace,
+             size_t workspace_bytes, attn_stream_t stream);
 
 /*
  * attn_device_status -- synchronises `stream`, then returns and clears the

@@ -204,3 +204,40 @@ def test_qk_rmsnorm_rejects_bad_arguments(lib, kw, code):
                             a["B"], a["Sq"], a["Sk"], a["Hq"], a["Hkv"], a["d"], a["eps"],
                             a["dtype"], stream=0)
     assert rc == code
+
+
+# ----------------------------------------------------------------- backward --
+
+def test_bwd_workspace_size():
+    # 2 fp32 per query row padded to whole 128-row tiles
+    assert ea.attn_bwd_workspace_size(2, 32, 8192) == (ea.ATTN_OK, 2 * 2 * 32 * 8192 * 4)
+    assert ea.attn_bwd_workspace_size(1, 3, 300) == (ea.ATTN_OK, 2 * 3 * 384 * 4)
+    assert ea.attn_bwd_workspace_size(1, 1, 1) == (ea.ATTN_OK, 2 * 128 * 4)
+    assert ea.attn_bwd_workspace_size(0, 1, 1)[0] == ea.ATTN_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(d_o=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(dk=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(o=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(lse=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace_bytes=2 * 4 * 128 * 4 - 4), ea.ATTN_ERR_INVALID_ARG),
+    (dict(workspace=0xC0008), ea.ATTN_ERR_MISALIGNED),
+    (dict(dq=0xA0004), ea.ATTN_ERR_MISALIGNED),
+    (dict(d_o=0x70002), ea.ATTN_ERR_MISALIGNED),
+    (dict(dtype=ea.ATTN_FP8_E4M3), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(Hkv=3), ea.ATTN_ERR_INVALID_ARG),
+    (dict(scale=0.0), ea.ATTN_ERR_INVALID_ARG),
+    (dict(Sk=0), ea.ATTN_ERR_INVALID_ARG),
+])
+def test_bwd_rejects_bad_arguments(lib, kw, code):
+    a = dict(q=Q, k=K, v=V, o=O, lse=L, d_o=0x70000, dq=0xA0000, dk=0xB0000, dv=0xD0000, B=1,
+             Hq=4, Hkv=2, Sq=100, Sk=100, d=128, causal=1, scale=0.1, dtype=ea.ATTN_BF16,
+             workspace=0xC0000, workspace_bytes=2 * 4 * 128 * 4)
+    a.update(kw)
+    rc = ea.attn_bwd(a["q"], a["k"], a["v"], a["o"], a["lse"], a["d_o"], a["dq"], a["dk"],
+                     a["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["d"], a["causal"],
+                     a["scale"], a["dtype"], a["workspace"], a["workspace_bytes"], stream=0)
+    assert rc == code
