@@ -7,7 +7,9 @@
 A step is one attention forward (one ``attn_fwd`` call through the C ABI)
 over the whole workload, inputs resident in device memory. The default
 workload is the long-context prefill shape B=2, H=32, S=8192, d=128, bf16,
-causal. Prints ONE JSON line on rank 0.
+causal. Workloads named ``bwd_*`` time the backward pass instead (one
+``attn_bwd`` call: dQ, dK, dV from q, k, v, O, LSE and dO), counted as 2.5
+times the forward's FLOPs. Prints ONE JSON line on rank 0.
 
 With N > 1 (one process per GPU, launched by torch.distributed.run) every rank
 runs the same workload on its own GPU (independent replicas: the heads of
@@ -33,6 +35,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = ("attention fwd TFLOP/s (4·B·H·Sq·Sk·d, causal halved) "
           "and % of B300 tensor peak")
+METRIC_BWD = ("attention bwd TFLOP/s (2.5 x 4·B·H·Sq·Sk·d, causal halved) "
+              "and % of B300 tensor peak")
+
+
+def metric_of(w) -> str:
+    return METRIC_BWD if w.backward else METRIC
 DEFAULT_WORKLOAD = "b2h32s8192d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
@@ -171,8 +179,11 @@ def _oracle_inputs(w):
         return {"dtype": "e4m3", "q": qc[0], "k": kc[0], "v": vc[0],
                 "q_scale": qc[1], "k_scale": kc[1], "v_scale": vc[1]}
     q, k, v = inputs.draw_workload_16(w)
-    return {"dtype": w.dtype, "q": inputs.bits16(q), "k": inputs.bits16(k),
+    bits = {"dtype": w.dtype, "q": inputs.bits16(q), "k": inputs.bits16(k),
             "v": inputs.bits16(v)}
+    if w.backward:
+        bits["do"] = inputs.bits16(inputs.draw_grad_out(w.B, w.Sq, w.Hq, w.d, w.seed, w.dtype))
+    return bits
 
 
 def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = None):
@@ -188,7 +199,7 @@ def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = No
             vis = np.clip(i + (w.Sk - w.Sq) + 1, 0, w.Sk)
         else:
             vis = np.full(rows.shape, w.Sk)
-        return float(4.0 * w.d * vis.sum())
+        return float(4.0 * w.d * vis.sum()) * (2.5 if w.backward else 1.0)
 
     rng = np.random.default_rng(seed)
     total = w.B * w.Hq * w.Sq
@@ -196,9 +207,13 @@ def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = No
     while True:
         rows = np.sort(rng.choice(total, size=min(n, total), replace=False)).astype(np.int64)
         t0 = time.perf_counter()
-        oracle.attn_fwd(bits["q"], bits["k"], bits["v"], w.causal, w.scale, dtype=bits["dtype"],
-                        q_scale=bits.get("q_scale"), k_scale=bits.get("k_scale"),
-                        v_scale=bits.get("v_scale"), rows=rows)
+        if w.backward:  # dQ of the sampled rows (each recomputes its O and LSE)
+            oracle.attn_bwd_sampled(bits["q"], bits["k"], bits["v"], bits["do"], w.causal,
+                                    w.scale, rows, np.zeros(0, np.int64), dtype=bits["dtype"])
+        else:
+            oracle.attn_fwd(bits["q"], bits["k"], bits["v"], w.causal, w.scale,
+                            dtype=bits["dtype"], q_scale=bits.get("q_scale"),
+                            k_scale=bits.get("k_scale"), v_scale=bits.get("v_scale"), rows=rows)
         dt = time.perf_counter() - t0
         if n_fixed or dt >= target_s or n >= total:
             return rows_flops(rows), dt, rows.size, int(os.environ["OMP_NUM_THREADS"])
@@ -210,7 +225,8 @@ def cpu_baseline(w, target_s: float = 12.0):
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
             "sample": f"{n} random query rows of all (b, h) of the workload "
                       f"({flops / 1e9:.1f} GFLOP by the metric's count) in {dt:.1f} s, "
-                      "fp64 two-pass oracle, OpenMP"}
+                      + ("fp64 oracle dQ rows (O, LSE recomputed per row), OpenMP"
+                         if w.backward else "fp64 two-pass oracle, OpenMP")}
 
 
 def run_reference(args, w):
@@ -229,7 +245,7 @@ def run_reference(args, w):
     tot_t = sum(t for _, t, _ in flops_t)
     value = tot_f / tot_t / 1e12
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "impl": "reference", "metric": metric_of(w), "value": value, "unit": "TFLOP/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(flops_t), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -272,6 +288,38 @@ def job_tflops(flops_per_step: float, steps: int, world: int, total_ms: float) -
 
 
 # ------------------------------------------------------------- GPU path --
+
+def e2e_backward(args, w, host, dev_in, o, lse, bwd, step, stream, dev, dist, world, flops):
+    """The backward step end to end: its inputs (q, k, v, O, LSE, dO) copied
+    from pinned host memory, attn_bwd, and dQ, dK, dV copied back, every step."""
+    import torch
+    h_o = o.cpu().pin_memory()
+    h_lse = lse.cpu().pin_memory()
+    hin = list(host) + [h_o, h_lse, bwd["h_do"]]
+    din = list(dev_in) + [o, lse, bwd["do"]]
+    hout = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in bwd["grads"]]
+    e_steps = max(3, min(args.steps, 20))
+    for it in range(e_steps + 2):
+        if it == 2:
+            if dist is not None:
+                dist.barrier()
+            torch.cuda.synchronize(dev)
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        for dst, src in zip(din, hin):
+            dst.copy_(src, non_blocking=True)
+        step()
+        for dst, src in zip(hout, bwd["grads"]):
+            dst.copy_(src, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    return {"value": job_tflops(flops, e_steps, world, e_ms), "unit": "TFLOP/s",
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
+            "ms_per_step": e_ms / e_steps}
+
 
 def run_ours(args, w):
     import torch
@@ -318,6 +366,25 @@ def run_ours(args, w):
         wbytes = nsplit * w.B * w.Hq * w.Sq * (w.d + 1) * 4
         ws = torch.empty(wbytes // 4, dtype=torch.float32, device=dev)
 
+    bwd = None
+    if w.backward:
+        # the backward pass's inputs: q, k, v, the forward's O and LSE on
+        # them, and dO (all resident); outputs dQ, dK, dV
+        code = ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16
+        h_do = inputs.draw_grad_out(w.B, w.Sq, w.Hq, w.d, w.seed, w.dtype).pin_memory()
+        d_o = h_do.to(dev)
+        q, k, v = dev_in
+        rc = ea.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal, w.scale,
+                         code, stream)
+        if rc != ea.ATTN_OK:
+            raise ea.AttnError(rc, "attn_fwd")
+        rc, wbytes = ea.attn_bwd_workspace_size(w.B, w.Hq, w.Sq)
+        if rc != ea.ATTN_OK:
+            raise ea.AttnError(rc, "attn_bwd_workspace_size")
+        bwd = {"code": code, "do": d_o, "h_do": h_do,
+               "grads": (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)),
+               "ws": torch.empty(wbytes // 4, dtype=torch.float32, device=dev)}
+
     norm = None
     if w.qknorm:
         wq = inputs.draw_norm_weights(w.Hq * w.d, w.seed + 50, w.dtype).to(dev)
@@ -334,6 +401,15 @@ def run_ours(args, w):
         return qn, kn
 
     def step():
+        if bwd is not None:
+            q, k, v = dev_in
+            dq, dk, dv = bwd["grads"]
+            rc = ea.attn_bwd(q, k, v, o, lse, bwd["do"], dq, dk, dv, w.B, w.Hq, w.Hkv, w.Sq,
+                             w.Sk, w.d, w.causal, w.scale, bwd["code"], bwd["ws"],
+                             bwd["ws"].numel() * 4, stream)
+            if rc != ea.ATTN_OK:
+                raise ea.AttnError(rc, "attn_bwd")
+            return
         if norm is not None:
             qn, kn = prologue()
             rc = ea.attn_fwd(qn, kn, dev_in[2], o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
@@ -394,7 +470,10 @@ def run_ours(args, w):
     # end to end through the public API: pinned host inputs -> device -> kernel
     # -> O and LSE back to pinned host memory, every step
     e2e = None
-    if host is not None:
+    if host is not None and bwd is not None:
+        e2e = e2e_backward(args, w, host, dev_in, o, lse, bwd, step, stream, dev, dist, world,
+                           flops)
+    elif host is not None:
         ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
         hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
         e_steps = max(3, min(args.steps, 20))
@@ -453,13 +532,19 @@ def run_ours(args, w):
 
     peaks, peaks_src = load_peaks()
     mean_launch_ms = statistics.mean(launch_ms)
-    achieved = flops / (mean_launch_ms * 1e-3) / 1e12
+    # the backward pass runs 7 matrix products per visible (query, key) pair
+    # (dK/dV kernel 4, dQ kernel 3) against the metric's 5
+    executed = flops * (7.0 / 5.0 if bwd is not None else 1.0)
+    achieved = executed / (mean_launch_ms * 1e-3) / 1e12
     peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak, "traffic": ncu_traffic(w.name),
-        "kernel": f"attn_fwd_kernel<{w.d},{str(w.dtype == 'e4m3').lower()},"
-                  f"{str(w.dtype == 'f16').lower()}>",
+        "kernel": (f"attn_bwd (bwd_prep_kernel + bwd_dkdv_kernel + bwd_dq_kernel)<{w.d},"
+                   f"{str(w.dtype == 'f16').lower()}>, executed FLOPs (7 products per pair)"
+                   if bwd is not None else
+                   f"attn_fwd_kernel<{w.d},{str(w.dtype == 'e4m3').lower()},"
+                   f"{str(w.dtype == 'f16').lower()}>"),
         "peak_source": (f"{peaks_src} bf16 burst" if w.dtype != "e4m3"
                         else f"{peaks_src} bf16 burst x 2 (nominal fp8/bf16 ratio)"),
         "frac_of_sustained": achieved / (peaks.get("bf16_tflops_sustained", peak) *
@@ -467,12 +552,13 @@ def run_ours(args, w):
         "launch_ms_median": statistics.median(launch_ms),
     }
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": metric_of(w), "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": w.dtype, "data": "synthetic",
         "config": workload_config(w, nsplit), "clocks": clocks.summary(), "e2e": e2e,
-        "gpu_launches": args.steps * (2 if (ws is not None or norm is not None) else 1),
+        "gpu_launches": args.steps * (3 if bwd is not None else
+                                      2 if (ws is not None or norm is not None) else 1),
         "roofline": roofline,
     }
     if prologue_line is not None:

@@ -38,15 +38,19 @@ class Workload:
     seed: int = 1000
     splits: int = 0              # split-KV ranges: 0 = plain forward, -1 = the plan's choice
     qknorm: bool = False         # RMSNorm across heads of Q and K before the attention
+    backward: bool = False       # the step is the backward pass (dQ, dK, dV) instead
 
     @property
     def scale(self) -> float:
         return 1.0 / math.sqrt(self.d)
 
     def flops(self) -> float:
-        """Metric FLOP count: 4*B*H*Sq*Sk*d, halved for causal."""
+        """Metric FLOP count of the forward pass: 4*B*H*Sq*Sk*d, halved for
+        causal; the backward pass counts 2.5 times that (its five matrix
+        products against the forward's two)."""
         f = 4.0 * self.B * self.Hq * self.Sq * self.Sk * self.d
-        return f / 2 if self.causal else f
+        f = f / 2 if self.causal else f
+        return 2.5 * f if self.backward else f
 
 
 # The five reference workloads (long-context prefill shapes); the seed is
@@ -72,6 +76,13 @@ WORKLOADS = {
     # the long-context prefill shape behind the QK-RMSNorm prologue
     "qknorm_b2h32s8192d128_causal": Workload("qknorm_b2h32s8192d128_causal", 2, 32, 32, 8192,
                                              8192, 128, True, seed=1002, qknorm=True),
+    # backward pass of the long-context prefill shape (same inputs, dO drawn
+    # from its own generator)
+    "bwd_b2h32s8192d128_causal": Workload("bwd_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192,
+                                          128, True, seed=1002, backward=True),
+    "bwd_gqa_b1hq32hkv8s16384d128_causal": Workload("bwd_gqa_b1hq32hkv8s16384d128_causal", 1, 32,
+                                                    8, 16384, 16384, 128, True, seed=1003,
+                                                    backward=True),
     # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
     "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
                                           True, dtype="f16", seed=1005),

@@ -62,6 +62,11 @@ def _load():
         lib.oracle_attn_bwd.restype = ctypes.c_int
         lib.oracle_attn_bwd.argtypes = ([ctypes.c_void_p] * 4 + [ctypes.c_int] + [ctypes.c_void_p] * 3
                                         + [ctypes.c_int] * 7 + [ctypes.c_double])
+        lib.oracle_attn_bwd_sampled.restype = ctypes.c_int
+        lib.oracle_attn_bwd_sampled.argtypes = (
+            [ctypes.c_void_p] * 4 + [ctypes.c_int] * 8 + [ctypes.c_double]
+            + [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64]
+            + [ctypes.c_void_p] * 3)
         lib.oracle_attn_fwd.restype = ctypes.c_int
         lib.oracle_attn_fwd.argtypes = (
             [ctypes.c_void_p] * 6 + [ctypes.c_int] + [ctypes.c_void_p] * 2
@@ -197,3 +202,33 @@ def attn_bwd(q, k, v, d_o, causal: bool, scale: float, dtype: str = "bf16"):
     if rc != 0:
         raise ValueError("oracle rejected the dimensions")
     return dq, dk, dv
+
+
+def attn_bwd_sampled(q, k, v, d_o, causal: bool, scale: float, qrows, krows, dtype: str = "bf16"):
+    """fp64 gradients at sampled positions: dq [len(qrows), d] for the query
+    rows (b*Hq + hq)*Sq + i and (dk, dv) [len(krows), d] for the keys
+    (b*Hkv + hk)*Sk + j, in the order given."""
+    lib = _load()
+    if dtype not in ("bf16", "f16"):
+        raise ValueError(f"unknown dtype {dtype!r}")
+    q, k, v, d_o = (np.ascontiguousarray(x).view(np.uint16) for x in (q, k, v, d_o))
+    B, Sq, Hq, d = q.shape
+    _, Sk, Hkv, _ = k.shape
+    qrows = np.ascontiguousarray(qrows, dtype=np.int64)
+    krows = np.asarray(krows, dtype=np.int64)
+    order = np.argsort(krows, kind="stable")
+    ks = np.ascontiguousarray(krows[order])
+    dq = np.empty((qrows.size, d), dtype=np.float64)
+    dk = np.empty((ks.size, d), dtype=np.float64)
+    dv = np.empty((ks.size, d), dtype=np.float64)
+    rc = lib.oracle_attn_bwd_sampled(_ptr(q), _ptr(k), _ptr(v), _ptr(d_o),
+                                     DTYPE_F16 if dtype == "f16" else DTYPE_BF16, B, Hq, Hkv,
+                                     Sq, Sk, d, int(bool(causal)), float(scale), _ptr(qrows),
+                                     qrows.size, _ptr(ks), ks.size, _ptr(dq), _ptr(dk), _ptr(dv))
+    if rc != 0:
+        raise ValueError("oracle rejected the dimensions or rows")
+    out_k = np.empty_like(dk)
+    out_v = np.empty_like(dv)
+    out_k[order] = dk
+    out_v[order] = dv
+    return dq, out_k, out_v

@@ -337,6 +337,122 @@ int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* d_o
     return 0;
 }
 
+/* Sampled form of oracle_attn_bwd, for inputs too large to differentiate
+ * whole: dq for the query rows qrows[r] = (b Hq + hq) Sq + i (out [nq, d]) and
+ * dk, dv for the keys krows[r] = (b Hkv + hk) Sk + j (out [nk, d]; krows
+ * sorted ascending). Same formulas as oracle_attn_bwd; LSE_i and D_i are
+ * recomputed for every row of the query heads a sampled key's KV head serves. */
+int oracle_attn_bwd_sampled(const void* q, const void* k, const void* v, const void* d_o,
+                            int dtype, int B, int Hq, int Hkv, int Sq, int Sk, int d, int causal,
+                            double scale, const int64_t* qrows, int64_t nq, const int64_t* krows,
+                            int64_t nk, double* dq, double* dk, double* dv) {
+    if (check_dims_bwd(B, Hq, Hkv, Sq, Sk, d)) return 1;
+    if (dtype != ORACLE_DTYPE_BF16 && dtype != ORACLE_DTYPE_F16) return 1;
+    for (int64_t r = 0; r < nq; ++r)
+        if (qrows[r] < 0 || qrows[r] >= (int64_t)B * Hq * Sq) return 1;
+    for (int64_t r = 0; r < nk; ++r) {
+        if (krows[r] < 0 || krows[r] >= (int64_t)B * Hkv * Sk) return 1;
+        if (r > 0 && krows[r] < krows[r - 1]) return 1;
+    }
+    oracle_inputs in = {q, k, v, NULL, NULL, NULL, dtype, B, Hq, Hkv, Sq, Sk, d};
+    oracle_inputs gin = {d_o, NULL, NULL, NULL, NULL, NULL, dtype, B, Hq, Hkv, Sq, Sk, d};
+    const int group = Hq / Hkv;
+    const long off = (long)Sk - (long)Sq; /* key j visible to row i iff j <= i + off */
+
+    /* dq rows */
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t r = 0; r < nq; ++r) {
+        const int i = (int)(qrows[r] % Sq);
+        const int bh = (int)(qrows[r] / Sq);
+        const int b = bh / Hq, hq = bh % Hq, hk = hq / group;
+        double* o_row = (double*)malloc(sizeof(double) * 2 * (size_t)d);
+        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+        double* dorow = o_row + d;
+        double* out = dq + (size_t)r * d;
+        const double lse = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+        double D = 0.0;
+        for (int c = 0; c < d; ++c) {
+            out[c] = 0.0;
+            dorow[c] = load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c);
+            D += dorow[c] * o_row[c];
+        }
+        if (lse != -INFINITY) {
+            long jmax = Sk - 1;
+            if (causal && (long)i + off < jmax) jmax = (long)i + off;
+            for (long j = 0; j <= jmax; ++j) {
+                double dot = 0.0, dp = 0.0;
+                for (int c = 0; c < d; ++c) {
+                    dot += load_elem(&in, q, NULL, Sq, Hq, b, i, hq, c) *
+                           load_elem(&in, k, NULL, Sk, Hkv, b, (int)j, hk, c);
+                    dp += dorow[c] * load_elem(&in, v, NULL, Sk, Hkv, b, (int)j, hk, c);
+                }
+                const double ds = exp(scale * dot - lse) * (dp - D);
+                for (int c = 0; c < d; ++c)
+                    out[c] += scale * ds * load_elem(&in, k, NULL, Sk, Hkv, b, (int)j, hk, c);
+            }
+        }
+        free(o_row);
+        free(work);
+    }
+
+    /* dk, dv keys, grouped by (b, hk) */
+    double* lse_all = (double*)malloc(sizeof(double) * (size_t)group * Sq);
+    double* D_all = (double*)malloc(sizeof(double) * (size_t)group * Sq);
+    int64_t r0 = 0;
+    while (r0 < nk) {
+        const int64_t bhk = krows[r0] / Sk;
+        int64_t r1 = r0;
+        while (r1 < nk && krows[r1] / Sk == bhk) ++r1;
+        const int b = (int)(bhk / Hkv), hk = (int)(bhk % Hkv);
+        /* row statistics of every query head served by this KV head */
+#pragma omp parallel for schedule(dynamic, 16)
+        for (long gi = 0; gi < (long)group * Sq; ++gi) {
+            const int g = (int)(gi / Sq), i = (int)(gi % Sq);
+            const int hq = hk * group + g;
+            double* o_row = (double*)malloc(sizeof(double) * (size_t)d);
+            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+            lse_all[gi] = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+            double D = 0.0;
+            for (int c = 0; c < d; ++c) D += load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c) * o_row[c];
+            D_all[gi] = D;
+            free(o_row);
+            free(work);
+        }
+#pragma omp parallel for schedule(dynamic, 1)
+        for (int64_t r = r0; r < r1; ++r) {
+            const int j = (int)(krows[r] % Sk);
+            double* ok = dk + (size_t)r * d;
+            double* ov = dv + (size_t)r * d;
+            for (int c = 0; c < d; ++c) ok[c] = ov[c] = 0.0;
+            for (int g = 0; g < group; ++g) {
+                const int hq = hk * group + g;
+                for (int i = 0; i < Sq; ++i) {
+                    if (causal && (long)j > (long)i + off) continue;
+                    const double lse = lse_all[(size_t)g * Sq + i];
+                    if (lse == -INFINITY) continue;
+                    double dot = 0.0, dp = 0.0;
+                    for (int c = 0; c < d; ++c) {
+                        dot += load_elem(&in, q, NULL, Sq, Hq, b, i, hq, c) *
+                               load_elem(&in, k, NULL, Sk, Hkv, b, j, hk, c);
+                        dp += load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c) *
+                              load_elem(&in, v, NULL, Sk, Hkv, b, j, hk, c);
+                    }
+                    const double p = exp(scale * dot - lse);
+                    const double ds = p * (dp - D_all[(size_t)g * Sq + i]);
+                    for (int c = 0; c < d; ++c) {
+                        ok[c] += scale * ds * load_elem(&in, q, NULL, Sq, Hq, b, i, hq, c);
+                        ov[c] += p * load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c);
+                    }
+                }
+            }
+        }
+        r0 = r1;
+    }
+    free(lse_all);
+    free(D_all);
+    return 0;
+}
+
 static int check_dims(int B, int Hq, int Hkv, int Sq, int Sk, int d) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Sk <= 0 || d <= 0) return 1;
     if (Hq % Hkv != 0) return 1;

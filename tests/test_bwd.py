@@ -124,3 +124,44 @@ def test_gqa_equals_mha_on_repeated_kv_heads():
     for a, b in ((dk1.float(), dk2s), (dv1.float(), dv2s)):
         tol = 2.0 ** -7 * b.abs() + 0.01 * b.abs().max()
         assert bool(((a - b).abs() <= tol).all())
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name,nkv", [("bwd_b2h32s8192d128_causal", 2),
+                                      ("bwd_gqa_b1hq32hkv8s16384d128_causal", 1)])
+def test_backward_full_size_sampled(oracle_mod, name, nkv):
+    """The bench's workloads at full size, in the bench's launch configuration:
+    dQ at sampled query rows (the first and last rows of the first and last
+    heads included) and dK, dV at sampled keys of nkv (batch, KV head) pairs
+    (the first and last keys included), against the sampled oracle. The
+    tolerance's max|ref| is taken over the sample, which holds the largest
+    gradients (the first rows and keys under the causal mask)."""
+    torch = require_gpu()
+    w = inputs.WORKLOADS[name]
+    q, k, v = inputs.draw_workload_16(w)
+    do = inputs.draw_grad_out(w.B, w.Sq, w.Hq, w.d, w.seed, w.dtype)
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = ea.forward(qd, kd, vd, causal=w.causal, scale=w.scale)
+    dq, dk, dv = ea.backward(qd, kd, vd, o, lse, dod, causal=w.causal, scale=w.scale)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    del o, lse, qd, kd, vd, dod
+    qrows = inputs.sample_rows(w.B, w.Hq, w.Sq, 48, seed=w.seed + 7)
+    rng = np.random.default_rng(w.seed + 8)
+    pairs = [0, w.B * w.Hkv - 1][:nkv]
+    krows = []
+    for bhk in pairs:
+        keys = set(int(x) for x in rng.choice(w.Sk, size=22, replace=False)) | {0, w.Sk - 1}
+        krows += [bhk * w.Sk + j for j in sorted(keys)]
+    krows = np.array(krows, dtype=np.int64)
+    rq, rk, rv = oracle_mod.attn_bwd_sampled(inputs.bits16(q), inputs.bits16(k),
+                                             inputs.bits16(v), inputs.bits16(do), w.causal,
+                                             w.scale, qrows, krows, dtype=w.dtype)
+
+    def gather(t, rows, H, S):  # flat (b*H + h)*S + s -> [n, d]
+        bh, s = rows // S, rows % S
+        b, h = bh // H, bh % H
+        return t[torch.as_tensor(b), torch.as_tensor(s), torch.as_tensor(h)].float().cpu().numpy()
+
+    assert_grad_close("dq", gather(dq, qrows, w.Hq, w.Sq), rq)
+    assert_grad_close("dk", gather(dk, krows, w.Hkv, w.Sk), rk)
+    assert_grad_close("dv", gather(dv, krows, w.Hkv, w.Sk), rv)

@@ -129,3 +129,22 @@ def test_shift_and_normalisation_invariants(oracle_mod, causal):
     np.testing.assert_allclose(dv.sum(axis=1), want, atol=1e-10)
     if causal:  # rows with no visible key get no gradient
         assert np.all(dq[:, ~seen] == 0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_sampled_gradients_equal_the_whole(oracle_mod, causal):
+    """The sampled form (used at sizes the whole oracle cannot finish) gives
+    the whole computation's values at the sampled rows and keys."""
+    B, Hq, Hkv, Sq, Sk, d = 2, 4, 2, 37, 53, 16
+    (qb, _), (kb, _), (vb, _), (dob, _) = make_case(13, B, Hq, Hkv, Sq, Sk, d)
+    dq, dk, dv = oracle_mod.attn_bwd(qb, kb, vb, dob, causal, 0.25)
+    rng = np.random.default_rng(2)
+    qrows = rng.choice(B * Hq * Sq, size=40, replace=False)
+    krows = rng.choice(B * Hkv * Sk, size=30, replace=False)  # unsorted on purpose
+    sq, sk, sv = oracle_mod.attn_bwd_sampled(qb, kb, vb, dob, causal, 0.25, qrows, krows)
+    dq_flat = dq.transpose(0, 2, 1, 3).reshape(-1, d)  # (b, hq, i) order
+    dk_flat = dk.transpose(0, 2, 1, 3).reshape(-1, d)
+    dv_flat = dv.transpose(0, 2, 1, 3).reshape(-1, d)
+    np.testing.assert_allclose(sq, dq_flat[qrows], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(sk, dk_flat[krows], rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(sv, dv_flat[krows], rtol=1e-12, atol=1e-14)
