@@ -248,13 +248,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       return ATTN_ERR_CUDA;
     di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
   }
-  CUtensorMap tq, tdo, tk, tv, tk64, tv64;
+  CUtensorMap tq, tdo, tk, tv;
   if (!encode_bshd(&tq, q, false, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
       !encode_bshd(&tdo, d_o, false, B, Sq, Hq, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
       !encode_bshd(&tk, k, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
-      !encode_bshd(&tv, v, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16) ||
-      !encode_bshd(&tk64, k, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_KV_ROWS, F16) ||
-      !encode_bshd(&tv64, v, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_KV_ROWS, F16))
+      !encode_bshd(&tv, v, false, B, Sk, Hkv, D, C::CHUNK_ELEMS, attnb3::BWD_TILE, F16))
     return ATTN_ERR_CUDA;
 
   const size_t sq_pad = bwd_sq_pad(Sq);
@@ -277,10 +275,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   P.nk = (Sk + attnb3::BWD_TILE - 1) / attnb3::BWD_TILE;
   P.kv_npair = (P.nk + 1) / 2;
   P.kv_items = B * Hkv * P.kv_npair;
-  P.n_qp = (Sq + attnb3::BWD_UNIT_ROWS - 1) / attnb3::BWD_UNIT_ROWS;
-  P.q_npair = (P.n_qp + 1) / 2;
+  P.q_npair = (P.nq + 1) / 2;
   P.q_items = B * Hq * P.q_npair;
-  P.nkv64 = (Sk + attnb3::BWD_KV_ROWS - 1) / attnb3::BWD_KV_ROWS;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.scale = scale;
   P.timeout_ns = kWaitLimitNs;
@@ -295,7 +291,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   const int gkv = P.kv_items < di->num_sms ? P.kv_items : di->num_sms;
   kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
   const int gq = P.q_items < di->num_sms ? P.q_items : di->num_sms;
-  kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk64, tv64, P);
+  kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -17,17 +17,23 @@
 //                    memory while the Q / dO tiles of every query head of the
 //                    group stream past; dK and dV accumulate in tensor memory
 //                    and are written once;
-//   bwd_dq_kernel    unit = (b, query head, 256 query rows) = two 128-row Q
-//                    tiles in ping-pong over 64-key K/V tiles (the forward's
-//                    structure), S and dP recomputed, dQ accumulating in
-//                    tensor memory.
+//   bwd_dq_kernel    unit = (b, query head, 128 query rows): Q and dO stay in
+//                    shared memory while 128-key K/V tiles stream past; S and
+//                    dP are recomputed, dQ accumulates in tensor memory.
+// Every product is a full M = 128, N = 128 (or N = d) tcgen05 MMA: a
+// half-width N = 64 product fetches the same A operand from shared memory for
+// half the math and runs well below the tensor rate. The element-wise stages
+// overlap the products instead: P (the exponentials) is formed while the
+// tensor cores compute dP, and dS while they compute dV (or the next S).
 // Computing dQ apart from dK / dV costs two more matrix products per tile
 // pair (7 instead of 5) but keeps every output a plain store: no fp32 dQ
 // accumulator round-trips through HBM and the results are deterministic.
 //
 // Both tensor-core kernels: one persistent CTA per SM, 320 threads --
-// warps 0-7 element-wise work in two warpgroups, warp 8 MMA issuer (lane 0)
-// and TMEM owner, warp 9 TMA producer (lane 0). P and dS are rounded to the
+// warps 0-7 element-wise work in two warpgroups (warpgroup h takes columns
+// [64 h, 64 h + 64) of each 128 x 128 score tile; a thread owns one TMEM
+// lane), warp 8 MMA issuer (lane 0) and TMEM owner, warp 9 TMA producer
+// (lane 0). P and dS are rounded to the
 // input type (bf16 / fp16) and handed to the next MMA from tensor memory.
 // Every mbarrier wait is bounded (ATTN_ERR_TIMEOUT, then drain and release),
 // as in the forward kernel.
@@ -44,10 +50,8 @@ namespace attnb3 {
 constexpr int BWD_THREADS = 320;
 constexpr int BWD_WARP_MMA = 8;
 constexpr int BWD_WARP_LOAD = 9;
-constexpr int BWD_TILE = 128;     // query rows per Q tile; keys per dK/dV unit
-constexpr int BWD_HALF = 64;      // query columns per element-wise warpgroup (dK/dV)
-constexpr int BWD_KV_ROWS = 64;   // keys per K/V tile of the dQ kernel
-constexpr int BWD_UNIT_ROWS = 256;
+constexpr int BWD_TILE = 128;     // rows of every Q, dO, K and V tile
+constexpr int BWD_HALF = 64;      // score columns per element-wise warpgroup
 constexpr int BWD_PREP_THREADS = 256;
 constexpr int BWD_STATUS_TIMEOUT = 5;  // ATTN_ERR_TIMEOUT
 constexpr float BWD_LOG2E = 1.4426950408889634f;
@@ -61,14 +65,12 @@ struct BwdParams {
   int B, Hq, Hkv, Sq, Sk, Sq_pad;
   int group;            // Hq / Hkv
   int causal;
-  int nq;               // ceil(Sq / 128) Q tiles
+  int nq;               // ceil(Sq / 128) Q tiles (dQ units per (b, hq))
   int nk;               // ceil(Sk / 128) key tiles (dK/dV units per (b, hkv))
   int kv_npair;         // ceil(nk / 2): dK/dV work items per (b, hkv)
   int kv_items;         // B * Hkv * kv_npair
-  int n_qp;             // ceil(Sq / 256): dQ units per (b, hq)
-  int q_npair;          // ceil(n_qp / 2)
+  int q_npair;          // ceil(nq / 2): dQ work items per (b, hq)
   int q_items;          // B * Hq * q_npair
-  int nkv64;            // ceil(Sk / 64) K/V tiles of the dQ kernel
   float scale_log2;     // softmax scale * log2(e)
   float scale;          // softmax scale (dQ and dK carry it)
   unsigned long long timeout_ns;
@@ -81,51 +83,51 @@ struct BwdCfg {
   static constexpr int CHUNK = 128;               // bytes of a swizzled row chunk (64 elements)
   static constexpr int CHUNK_ELEMS = 64;
   static constexpr int NCHUNK = D / CHUNK_ELEMS;
-  static constexpr int TILE128 = 128 * D * 2;     // 128 rows of one head
-  static constexpr int CH128 = 128 * CHUNK;       // one 64-column chunk of those rows
-  static constexpr int TILE64 = 64 * D * 2;       // 64 rows
-  static constexpr int CH64 = 64 * CHUNK;
+  static constexpr int TILE = 128 * D * 2;        // 128 rows of one head
+  static constexpr int CH = 128 * CHUNK;          // one 64-column chunk of those rows
   static constexpr int KSTEPS_D = D / 16;         // 16 elements (32 bytes) per MMA
-  static constexpr uint32_t IDESC_N64 = make_idesc(128, 64, FMT, false);
-  static constexpr uint32_t IDESC_ACC = make_idesc(128, D, FMT, true);
+  static constexpr uint32_t IDESC_S = make_idesc(128, 128, FMT, false);  // S, dP (and transposes)
+  static constexpr uint32_t IDESC_ACC = make_idesc(128, D, FMT, true);   // dV, dK, dQ
   static constexpr int TMEM_COLS = 512;
   static constexpr int SMEM_ALLOC = 227 * 1024;
   // ---- dK/dV kernel: K, V, then NSTAGE stages of (Q, dO, lse2[128], D[128])
   static constexpr int NSTAGE = D == 128 ? 2 : 4;
-  static constexpr int STAGE = 2 * TILE128 + 1024;
+  static constexpr int STAGE = 2 * TILE + 1024;
   static constexpr int KV_OFF_K = 0;
-  static constexpr int KV_OFF_V = TILE128;
-  static constexpr int KV_OFF_ST = 2 * TILE128;
+  static constexpr int KV_OFF_V = TILE;
+  static constexpr int KV_OFF_ST = 2 * TILE;
   static constexpr int KV_OFF_BAR = KV_OFF_ST + NSTAGE * STAGE;
-  // kv_full, kv_empty, st_full[NSTAGE], st_empty[NSTAGE], sd_full[2],
-  // e_full[2], acc_full, acc_empty, drain
-  static constexpr int KV_NBAR = 2 + 2 * NSTAGE + 4 + 3;
+  // kv_full, kv_empty, st_full[NSTAGE], st_empty[NSTAGE], s_full, dp_full,
+  // p_full, ds_full, acc_full, drain
+  static constexpr int KV_NBAR = 2 + 2 * NSTAGE + 6;
   static constexpr int KV_OFF_MISC = KV_OFF_BAR + KV_NBAR * 8;
   static constexpr int KV_SMEM = KV_OFF_MISC + 16 + 1024;
-  // TMEM columns: S^T [0,128) (half h at 64 h; P^T packed into its first 32),
-  // dP^T [128,256) (dS^T packed likewise), dV, dK
+  // TMEM: S^T [0,128) (P^T packed into the first 32 columns of each 64-column
+  // half), dP^T [128,256) (dS^T packed likewise), dV, dK
   static constexpr int COL_ST = 0;
   static constexpr int COL_DPT = 128;
   static constexpr int COL_DV = 256;
   static constexpr int COL_DK = 256 + D;
-  // ---- dQ kernel: 2 Q tiles, 2 dO tiles, NSLOT 64-key K/V slots
-  static constexpr int NSLOT = D == 128 ? 6 : 8;
+  // ---- dQ kernel: Q, dO, then an NSLOT ring of 128-key K and V tiles
+  static constexpr int NSLOT = D == 128 ? 5 : 10;
   static constexpr int Q_OFF_Q = 0;
-  static constexpr int Q_OFF_DO = 2 * TILE128;
-  static constexpr int Q_OFF_KV = 4 * TILE128;
-  static constexpr int Q_OFF_BAR = Q_OFF_KV + NSLOT * TILE64;
-  // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], sd_full[2], e_full[2],
-  // dq_full[2], drain
-  static constexpr int Q_NBAR = 2 + 2 * NSLOT + 6 + 1;
+  static constexpr int Q_OFF_DO = TILE;
+  static constexpr int Q_OFF_KV = 2 * TILE;
+  static constexpr int Q_OFF_BAR = Q_OFF_KV + NSLOT * TILE;
+  // q_full, q_empty, kv_full[NSLOT], kv_empty[NSLOT], s_full[2], dp_full,
+  // ds_full, dq_full, drain
+  static constexpr int Q_NBAR = 2 + 2 * NSLOT + 6;
   static constexpr int Q_OFF_MISC = Q_OFF_BAR + Q_NBAR * 8;
   static constexpr int Q_SMEM = Q_OFF_MISC + 16 + 1024;
-  // TMEM columns of Q tile t: S [128 t, +64) (dS packed into its first 32),
-  // dP [128 t + 64, +64), dQ [256 + t d, +d)
+  // TMEM: S in two buffers [0,128) and [384,512) (dS packed into the first 32
+  // columns of each 64-column half), dP [128,256), dQ [256,256+d)
+  static constexpr int COL_SB0 = 0;
+  static constexpr int COL_SB1 = 384;
+  static constexpr int COL_DP = 128;
   static constexpr int COL_DQ = 256;
   static_assert(D == 64 || D == 128, "head dim");
   static_assert(KV_SMEM <= SMEM_ALLOC && Q_SMEM <= SMEM_ALLOC, "shared memory budget");
-  static_assert(COL_DK + D <= TMEM_COLS && COL_DQ + 2 * D <= TMEM_COLS, "TMEM budget");
-  static_assert(NSLOT % 2 == 0, "K/V slots alternate");
+  static_assert(COL_DK + D <= TMEM_COLS && COL_DQ + D <= COL_SB1, "TMEM budget");
 };
 
 // 1-D bulk copy global -> shared (both 16-byte aligned, bytes a multiple of
@@ -178,21 +180,18 @@ __device__ __forceinline__ uint32_t pack16x2(bool f16, float lo, float hi) {
 
 // ------------------------------------------------------------ MMA helpers --
 
-// D[tmem] = A * B^T with A = 128 rows (K-major, 128-row tile in 64-column
-// swizzled chunks) and B = 64 rows starting at row b_row0 of a tile whose
-// chunks are b_chunk bytes apart; N = 64, K = d.
+// D[tmem] = A * B^T with A and B two 128-row tiles (K-major, in 64-column
+// swizzled chunks of 128 rows); M = N = 128, K = d.
 template <int D, bool F16>
-__device__ __forceinline__ void issue_n64(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem,
-                                          uint32_t b_chunk, int b_row0) {
+__device__ __forceinline__ void issue_s128(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   using C = BwdCfg<D, F16>;
 #pragma unroll
   for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
     const uint32_t byte_k = ks * 32;
-    const uint32_t chunk = byte_k / C::CHUNK, within = byte_k % C::CHUNK;
-    const uint64_t a = make_sdesc(a_smem + chunk * C::CH128 + within, 16, 8 * C::CHUNK, 2u);
-    const uint64_t b = make_sdesc(b_smem + chunk * b_chunk + b_row0 * C::CHUNK + within, 16,
-                                  8 * C::CHUNK, 2u);
-    mma_f16_ss(d_tmem, a, b, C::IDESC_N64, ks > 0 ? 1u : 0u);
+    const uint32_t off = (byte_k / C::CHUNK) * C::CH + byte_k % C::CHUNK;
+    const uint64_t a = make_sdesc(a_smem + off, 16, 8 * C::CHUNK, 2u);
+    const uint64_t b = make_sdesc(b_smem + off, 16, 8 * C::CHUNK, 2u);
+    mma_f16_ss(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
   }
 }
 
@@ -323,11 +322,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t BAR_KV_EMPTY = bar0 + 8;
   const uint32_t BAR_ST_FULL = bar0 + 16;                       // + 8 * stage
   const uint32_t BAR_ST_EMPTY = BAR_ST_FULL + 8 * C::NSTAGE;    // + 8 * stage
-  const uint32_t BAR_SD_FULL = BAR_ST_EMPTY + 8 * C::NSTAGE;    // + 8 * half
-  const uint32_t BAR_E_FULL = BAR_SD_FULL + 16;                 // + 8 * half
-  const uint32_t BAR_ACC_FULL = BAR_E_FULL + 16;
-  const uint32_t BAR_ACC_EMPTY = BAR_ACC_FULL + 8;
-  const uint32_t BAR_DRAIN = BAR_ACC_EMPTY + 8;
+  const uint32_t BAR_S_FULL = BAR_ST_EMPTY + 8 * C::NSTAGE;
+  const uint32_t BAR_DP_FULL = BAR_S_FULL + 8;
+  const uint32_t BAR_P_FULL = BAR_DP_FULL + 8;
+  const uint32_t BAR_DS_FULL = BAR_P_FULL + 8;
+  const uint32_t BAR_ACC_FULL = BAR_DS_FULL + 8;
+  const uint32_t BAR_DRAIN = BAR_ACC_FULL + 8;
   volatile BwdCtl* ctl = reinterpret_cast<volatile BwdCtl*>(smem + C::KV_OFF_MISC);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -339,12 +339,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(BAR_ST_FULL + 8 * s, 1);
       mbar_init(BAR_ST_EMPTY + 8 * s, 1);
     }
-    for (int h = 0; h < 2; ++h) {
-      mbar_init(BAR_SD_FULL + 8 * h, 1);
-      mbar_init(BAR_E_FULL + 8 * h, 4);  // one elected arrive per warp of the half
-    }
+    mbar_init(BAR_S_FULL, 1);
+    mbar_init(BAR_DP_FULL, 1);
+    mbar_init(BAR_P_FULL, 8);   // one elected arrive per element-wise warp
+    mbar_init(BAR_DS_FULL, 8);
     mbar_init(BAR_ACC_FULL, 1);
-    mbar_init(BAR_ACC_EMPTY, 8);  // every element-wise warp, after its epilogue
     mbar_init(BAR_DRAIN, 1);
     ctl->abort_flag = 0u;
     fence_barrier_init();
@@ -374,13 +373,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (st == 0) break;
         if (st == 1 || U.T == 0) continue;
         if (!bwd_wait(BAR_KV_EMPTY, (u & 1u) ^ 1u, ctl, P)) { ok = false; break; }
-        mbar_arrive_expect_tx(BAR_KV_FULL, 2 * C::TILE128);
+        mbar_arrive_expect_tx(BAR_KV_FULL, 2 * C::TILE);
 #pragma unroll
         for (int c = 0; c < C::NCHUNK; ++c) {
-          tma_load_4d(sbase + C::KV_OFF_K + c * C::CH128, &tm_k, BAR_KV_FULL,
-                      c * C::CHUNK_ELEMS, U.hkv, U.key0, U.b);
-          tma_load_4d(sbase + C::KV_OFF_V + c * C::CH128, &tm_v, BAR_KV_FULL,
-                      c * C::CHUNK_ELEMS, U.hkv, U.key0, U.b);
+          tma_load_4d(sbase + C::KV_OFF_K + c * C::CH, &tm_k, BAR_KV_FULL, c * C::CHUNK_ELEMS,
+                      U.hkv, U.key0, U.b);
+          tma_load_4d(sbase + C::KV_OFF_V + c * C::CH, &tm_v, BAR_KV_FULL, c * C::CHUNK_ELEMS,
+                      U.hkv, U.key0, U.b);
         }
         ++u;
         for (int t = 0; t < U.T; ++t) {
@@ -393,18 +392,17 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           const int hq = U.hkv * P.group + g;
           const uint32_t stg = stage_smem(n);
           const uint32_t bar = BAR_ST_FULL + 8 * s;
-          mbar_arrive_expect_tx(bar, 2 * C::TILE128 + 1024);
+          mbar_arrive_expect_tx(bar, 2 * C::TILE + 1024);
 #pragma unroll
           for (int c = 0; c < C::NCHUNK; ++c) {
-            tma_load_4d(stg + c * C::CH128, &tm_q, bar, c * C::CHUNK_ELEMS, hq, qi * BWD_TILE,
-                        U.b);
-            tma_load_4d(stg + C::TILE128 + c * C::CH128, &tm_do, bar, c * C::CHUNK_ELEMS, hq,
+            tma_load_4d(stg + c * C::CH, &tm_q, bar, c * C::CHUNK_ELEMS, hq, qi * BWD_TILE, U.b);
+            tma_load_4d(stg + C::TILE + c * C::CH, &tm_do, bar, c * C::CHUNK_ELEMS, hq,
                         qi * BWD_TILE, U.b);
           }
           const size_t row = (static_cast<size_t>(U.b) * P.Hq + hq) * P.Sq_pad +
                              static_cast<size_t>(qi) * BWD_TILE;
-          bulk_load(stg + 2 * C::TILE128, P.lse2 + row, 512, bar);
-          bulk_load(stg + 2 * C::TILE128 + 512, P.dsum + row, 512, bar);
+          bulk_load(stg + 2 * C::TILE, P.lse2 + row, 512, bar);
+          bulk_load(stg + 2 * C::TILE + 512, P.dsum + row, 512, bar);
           ++n;
         }
       }
@@ -416,68 +414,63 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncwarp();
   } else if (warp == BWD_WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    // Per Q tile t and half h (64 queries):
-    //   S^T_h = K Q_h^T, dP^T_h = V dO_h^T         -> sd_full[h]
-    //   (element-wise: P^T_h, dS^T_h into TMEM)    <- e_full[h]
-    //   dV += P^T_h dO_h,  dK += dS^T_h Q_h
-    // issued as  SD(t,0) SD(t,1) | ACC(t,0) SD(t+1,0) | ACC(t,1) SD(t+1,1) | ...
-    // so each half's element-wise work overlaps the other half's MMAs;
-    // in-order execution makes SD(t+1,h) wait for ACC(t,h), which reads the
-    // same TMEM columns.
+    // Per Q tile t (all products M = 128; S^T and dP^T N = 128, the rest N = d):
+    //   S^T = K Q^T -> s_full;  dP^T = V dO^T -> dp_full
+    //   <- p_full (both warpgroups wrote P^T):  dV += P^T dO (two 64-query halves)
+    //   S^T(t+1)   (its columns held P^T(t); in-order execution puts it after
+    //               the dV products that read them)
+    //   <- ds_full:  dK += dS^T Q;  release the stage;  dP^T(t+1)
+    // The element-wise warps form P(t) while the tensor cores run dP^T(t), and
+    // dS(t) while they run dV(t) and S^T(t+1). The first products of a unit
+    // overwrite dV and dK; they wait for p_full of that unit, which both
+    // warpgroups arrive on only after their epilogue of the previous unit.
     if (lane == 0) {
-      uint32_t n = 0, u = 0, e[2] = {0u, 0u};
+      uint32_t n = 0, u = 0, pc = 0, dc = 0;
       bool ok = true;
       const uint32_t k_s = sbase + C::KV_OFF_K, v_s = sbase + C::KV_OFF_V;
-      auto issue_sd = [&](uint32_t nn, int h) {
-        const uint32_t stg = stage_smem(nn);
-        issue_n64<D, F16>(tmem + C::COL_ST + BWD_HALF * h, k_s, stg, C::CH128, BWD_HALF * h);
-        issue_n64<D, F16>(tmem + C::COL_DPT + BWD_HALF * h, v_s, stg + C::TILE128, C::CH128,
-                          BWD_HALF * h);
-        tc_commit(BAR_SD_FULL + 8 * h);
+      auto wait_stage = [&](uint32_t nn) {
+        return bwd_wait(BAR_ST_FULL + 8 * (nn % C::NSTAGE), (nn / C::NSTAGE) & 1u, ctl, P);
       };
       for (int i = 0; ok; ++i) {
         KvUnit U;
         const int st = kv_unit(i, P, U);
         if (st == 0) break;
         if (st == 1 || U.T == 0) continue;
-        if (!bwd_wait(BAR_KV_FULL, u & 1u, ctl, P)) { ok = false; break; }
-        if (!bwd_wait(BAR_ST_FULL + 8 * (n % C::NSTAGE), (n / C::NSTAGE) & 1u, ctl, P)) {
-          ok = false;
-          break;
-        }
+        if (!bwd_wait(BAR_KV_FULL, u & 1u, ctl, P) || !wait_stage(n)) { ok = false; break; }
         tc_fence_after();
-        issue_sd(n, 0);
-        issue_sd(n, 1);
-        for (int t = 0; ok && t < U.T; ++t) {
+        issue_s128<D, F16>(tmem + C::COL_ST, k_s, stage_smem(n));
+        tc_commit(BAR_S_FULL);
+        issue_s128<D, F16>(tmem + C::COL_DPT, v_s, stage_smem(n) + C::TILE);
+        tc_commit(BAR_DP_FULL);
+        for (int t = 0; t < U.T; ++t) {
           const uint32_t nn = n + t;
           const uint32_t stg = stage_smem(nn);
-          for (int h = 0; h < 2; ++h) {
-            if (!bwd_wait(BAR_E_FULL + 8 * h, e[h] & 1u, ctl, P)) { ok = false; break; }
-            ++e[h];
-            // the first products of a unit overwrite dV / dK: the previous
-            // unit's epilogue must have read them
-            if (t == 0 && h == 0 && !bwd_wait(BAR_ACC_EMPTY, (u & 1u) ^ 1u, ctl, P)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const bool acc = !(t == 0 && h == 0);
+          const bool more = t + 1 < U.T;
+          const bool acc = t > 0;
+          if (!bwd_wait(BAR_P_FULL, pc & 1u, ctl, P)) { ok = false; break; }
+          ++pc;
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
             issue_acc64<D, F16>(tmem + C::COL_DV, tmem + C::COL_ST + BWD_HALF * h,
-                                stg + C::TILE128, C::CH128, BWD_HALF * h, acc);
-            issue_acc64<D, F16>(tmem + C::COL_DK, tmem + C::COL_DPT + BWD_HALF * h, stg,
-                                C::CH128, BWD_HALF * h, acc);
-            if (h == 1) tc_commit(BAR_ST_EMPTY + 8 * (nn % C::NSTAGE));
-            if (t + 1 < U.T) {
-              if (h == 0) {
-                if (!bwd_wait(BAR_ST_FULL + 8 * ((nn + 1) % C::NSTAGE),
-                              ((nn + 1) / C::NSTAGE) & 1u, ctl, P)) {
-                  ok = false;
-                  break;
-                }
-                tc_fence_after();
-              }
-              issue_sd(nn + 1, h);
-            }
+                                stg + C::TILE, C::CH, BWD_HALF * h, acc || h > 0);
+          if (more) {
+            if (!wait_stage(nn + 1)) { ok = false; break; }
+            tc_fence_after();
+            issue_s128<D, F16>(tmem + C::COL_ST, k_s, stage_smem(nn + 1));
+            tc_commit(BAR_S_FULL);
+          }
+          if (!bwd_wait(BAR_DS_FULL, dc & 1u, ctl, P)) { ok = false; break; }
+          ++dc;
+          tc_fence_after();
+#pragma unroll
+          for (int h = 0; h < 2; ++h)
+            issue_acc64<D, F16>(tmem + C::COL_DK, tmem + C::COL_DPT + BWD_HALF * h, stg, C::CH,
+                                BWD_HALF * h, acc || h > 0);
+          tc_commit(BAR_ST_EMPTY + 8 * (nn % C::NSTAGE));
+          if (more) {
+            issue_s128<D, F16>(tmem + C::COL_DPT, v_s, stage_smem(nn + 1) + C::TILE);
+            tc_commit(BAR_DP_FULL);
           }
         }
         if (!ok) break;
@@ -498,8 +491,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int quad = warp & 3;
     const int rloc = quad * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t col_s = C::COL_ST + BWD_HALF * h, col_dp = C::COL_DPT + BWD_HALF * h;
     const float cs = P.scale_log2;
-    uint32_t n = 0, u = 0, sd = 0;
+    uint32_t n = 0, u = 0, sc = 0, dc = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
       KvUnit U;
@@ -521,8 +515,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       }
       for (int t = 0; t < U.T; ++t) {
         const uint32_t nn = n + t;
-        bool w = bwd_wait(BAR_SD_FULL + 8 * h, sd & 1u, ctl, P);
-        ++sd;
+        bool w = bwd_wait(BAR_S_FULL, sc & 1u, ctl, P);
+        ++sc;
         // lse2 / D of this tile were staged by TMA on st_full (already
         // complete: the MMA waited for it before issuing S^T)
         w = w && bwd_wait(BAR_ST_FULL + 8 * (nn % C::NSTAGE), (nn / C::NSTAGE) & 1u, ctl, P);
@@ -535,58 +529,79 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         int cmin = 0;
         if (!row_ok) cmin = BWD_HALF;
         else if (P.causal) cmin = kr - (P.Sk - P.Sq) - q0;
-        uint32_t sr[64], dr[64];
+        const uint32_t lse_s = stage_smem(nn) + 2 * C::TILE + 4 * BWD_HALF * h;
+        const uint32_t dsum_s = lse_s + 512;
+        float p[64];
         {
+          uint32_t sr[64];
           uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
           uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
-          uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr);
-          uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr + 32);
-          tmem_ld32_async(t_lane + C::COL_ST + BWD_HALF * h, s0);
-          tmem_ld32_async(t_lane + C::COL_ST + BWD_HALF * h + 32, s1);
-          tmem_ld32_async(t_lane + C::COL_DPT + BWD_HALF * h, d0);
-          tmem_ld32_async(t_lane + C::COL_DPT + BWD_HALF * h + 32, d1);
+          tmem_ld32_async(t_lane + col_s, s0);
+          tmem_ld32_async(t_lane + col_s + 32, s1);
           tmem_ld_wait();
           reg_fence(s0);
           reg_fence(s1);
-          reg_fence(d0);
-          reg_fence(d1);
-        }
-        const uint32_t lse_s = stage_smem(nn) + 2 * C::TILE128 + 4 * BWD_HALF * h;
-        const uint32_t dsum_s = lse_s + 512;
-        uint32_t pp[32], pd[32];
+          uint32_t pk[32];
 #pragma unroll
-        for (int c4 = 0; c4 < 16; ++c4) {
-          const uint4 l4 = lds128(lse_s + 16 * c4);
-          const uint4 d4 = lds128(dsum_s + 16 * c4);
-          const float lv[4] = {__uint_as_float(l4.x), __uint_as_float(l4.y),
-                               __uint_as_float(l4.z), __uint_as_float(l4.w)};
-          const float dv4[4] = {__uint_as_float(d4.x), __uint_as_float(d4.y),
-                                __uint_as_float(d4.z), __uint_as_float(d4.w)};
-          float p[4], ds[4];
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const uint4 l4 = lds128(lse_s + 16 * c4);
+            const float lv[4] = {__uint_as_float(l4.x), __uint_as_float(l4.y),
+                                 __uint_as_float(l4.z), __uint_as_float(l4.w)};
 #pragma unroll
-          for (int e2 = 0; e2 < 4; ++e2) {
-            const int c = 4 * c4 + e2;
-            float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -lv[e2]));
-            x = c < cmin ? 0.f : x;
-            p[e2] = x;
-            ds[e2] = x * (__uint_as_float(dr[c]) - dv4[e2]);
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
+              p[c] = c < cmin ? 0.f : x;
+            }
+            pk[2 * c4] = pack16x2(F16, p[4 * c4], p[4 * c4 + 1]);
+            pk[2 * c4 + 1] = pack16x2(F16, p[4 * c4 + 2], p[4 * c4 + 3]);
           }
-          pp[2 * c4] = pack16x2(F16, p[0], p[1]);
-          pp[2 * c4 + 1] = pack16x2(F16, p[2], p[3]);
-          pd[2 * c4] = pack16x2(F16, ds[0], ds[1]);
-          pd[2 * c4 + 1] = pack16x2(F16, ds[2], ds[3]);
+          tmem_st32(t_lane + col_s, pk);
+          tmem_st_wait();
         }
-        tmem_st32(t_lane + C::COL_ST + BWD_HALF * h, pp);
-        tmem_st32(t_lane + C::COL_DPT + BWD_HALF * h, pd);
-        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR_E_FULL + 8 * h);
+        if (lane == 0) mbar_arrive(BAR_P_FULL);
+
+        w = bwd_wait(BAR_DP_FULL, dc & 1u, ctl, P);
+        ++dc;
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t dr[64];
+          uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr);
+          uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr + 32);
+          tmem_ld32_async(t_lane + col_dp, d0);
+          tmem_ld32_async(t_lane + col_dp + 32, d1);
+          tmem_ld_wait();
+          reg_fence(d0);
+          reg_fence(d1);
+          uint32_t pd[32];
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const uint4 d4 = lds128(dsum_s + 16 * c4);
+            const float dv4[4] = {__uint_as_float(d4.x), __uint_as_float(d4.y),
+                                  __uint_as_float(d4.z), __uint_as_float(d4.w)};
+            float ds[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c = 4 * c4 + e;
+              ds[e] = p[c] * (__uint_as_float(dr[c]) - dv4[e]);
+            }
+            pd[2 * c4] = pack16x2(F16, ds[0], ds[1]);
+            pd[2 * c4 + 1] = pack16x2(F16, ds[2], ds[3]);
+          }
+          tmem_st32(t_lane + col_dp, pd);
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR_DS_FULL);
       }
       if (!ok) break;
       // ------------------------------------------------------ epilogue
       // warpgroup 0 writes dV, warpgroup 1 dK (times the softmax scale)
-      bool w = bwd_wait(BAR_ACC_FULL, u & 1u, ctl, P);
+      const bool w = bwd_wait(BAR_ACC_FULL, u & 1u, ctl, P);
       if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
       tc_fence_after();
       const float mul = h ? P.scale : 1.f;
@@ -608,8 +623,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
       }
       tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR_ACC_EMPTY);
       n += U.T;
       ++u;
     }
@@ -627,38 +640,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
 struct QUnit {
   int b, hq, hkv, row0;
-  int n[2];  // 64-key K/V tiles seen by Q tile 0 / 1 (0 = idle or fully masked)
-  int nmax;
+  int n;  // 128-key K/V tiles seen by the unit's rows (0 = every row fully masked)
 };
 
-// The i-th dQ unit of this CTA (the forward's pair order: level n_qp-1-p
-// with level p of the same (b, hq), heads innermost): 0 = none left,
-// 1 = skip, 2 = U filled.
+// The i-th dQ unit of this CTA: 0 = none left, 1 = skip, 2 = U filled. Work
+// item w = (b, hq, p) pairs Q tile nq-1-p (the most keys under a causal mask)
+// with Q tile p, so items cost about the same; query heads innermost, so the
+// CTAs in flight share a few KV heads' K and V in L2.
 __device__ __forceinline__ int q_unit(int i, const BwdParams& P, QUnit& U) {
   const int w = blockIdx.x + (i >> 1) * gridDim.x;
   if (w >= P.q_items) return 0;
   const int bh = w / P.q_npair, p = w - bh * P.q_npair;
-  const int level = (i & 1) ? p : P.n_qp - 1 - p;
-  if ((i & 1) && level == P.n_qp - 1 - p) return 1;
+  const int qi = (i & 1) ? p : P.nq - 1 - p;
+  if ((i & 1) && qi == P.nq - 1 - p) return 1;  // odd nq: the middle tile
   U.b = bh / P.Hq;
   U.hq = bh - U.b * P.Hq;
   U.hkv = U.hq / P.group;
-  U.row0 = level * BWD_UNIT_ROWS;
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const int r0 = U.row0 + t * BWD_TILE;
-    int n = 0;
-    if (r0 < P.Sq) {
-      if (!P.causal) {
-        n = P.nkv64;
-      } else {
-        const int lim = min(r0 + BWD_TILE, P.Sq) - 1 + (P.Sk - P.Sq) + 1;  // keys seen by the last row
-        n = lim <= 0 ? 0 : min((lim + BWD_KV_ROWS - 1) / BWD_KV_ROWS, P.nkv64);
-      }
-    }
-    U.n[t] = n;
+  U.row0 = qi * BWD_TILE;
+  U.n = P.nk;
+  if (P.causal) {
+    const int lim = min(U.row0 + BWD_TILE, P.Sq) + (P.Sk - P.Sq);  // keys seen by the last row
+    U.n = lim <= 0 ? 0 : min((lim + BWD_TILE - 1) / BWD_TILE, P.nk);
   }
-  U.nmax = max(U.n[0], U.n[1]);
   return 2;
 }
 
@@ -666,8 +669,8 @@ template <int D, bool F16>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q,
                   const __grid_constant__ CUtensorMap tm_do,
-                  const __grid_constant__ CUtensorMap tm_k64,
-                  const __grid_constant__ CUtensorMap tm_v64, const BwdParams P) {
+                  const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_v, const BwdParams P) {
   using C = BwdCfg<D, F16>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -678,10 +681,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   const uint32_t BAR_Q_EMPTY = bar0 + 8;
   const uint32_t BAR_KV_FULL = bar0 + 16;                    // + 8 * slot
   const uint32_t BAR_KV_EMPTY = BAR_KV_FULL + 8 * C::NSLOT;  // + 8 * slot
-  const uint32_t BAR_SD_FULL = BAR_KV_EMPTY + 8 * C::NSLOT;  // + 8 * t
-  const uint32_t BAR_E_FULL = BAR_SD_FULL + 16;              // + 8 * t
-  const uint32_t BAR_DQ_FULL = BAR_E_FULL + 16;              // + 8 * t
-  const uint32_t BAR_DRAIN = BAR_DQ_FULL + 16;
+  const uint32_t BAR_S_FULL = BAR_KV_EMPTY + 8 * C::NSLOT;   // + 8 * S buffer
+  const uint32_t BAR_DP_FULL = BAR_S_FULL + 16;
+  const uint32_t BAR_DS_FULL = BAR_DP_FULL + 8;
+  const uint32_t BAR_DQ_FULL = BAR_DS_FULL + 8;
+  const uint32_t BAR_DRAIN = BAR_DQ_FULL + 8;
   volatile BwdCtl* ctl = reinterpret_cast<volatile BwdCtl*>(smem + C::Q_OFF_MISC);
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -693,18 +697,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       mbar_init(BAR_KV_FULL + 8 * s, 1);
       mbar_init(BAR_KV_EMPTY + 8 * s, 1);
     }
-    for (int t = 0; t < 2; ++t) {
-      mbar_init(BAR_SD_FULL + 8 * t, 1);
-      mbar_init(BAR_E_FULL + 8 * t, 4);
-      mbar_init(BAR_DQ_FULL + 8 * t, 1);
-    }
+    mbar_init(BAR_S_FULL, 1);
+    mbar_init(BAR_S_FULL + 8, 1);
+    mbar_init(BAR_DP_FULL, 1);
+    mbar_init(BAR_DS_FULL, 8);  // one elected arrive per element-wise warp
+    mbar_init(BAR_DQ_FULL, 1);
     mbar_init(BAR_DRAIN, 1);
     ctl->abort_flag = 0u;
     fence_barrier_init();
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_k64);
-    tma_prefetch_desc(&tm_v64);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
   }
   if (warp == BWD_WARP_MMA) {
     tmem_alloc(sbase + C::Q_OFF_MISC, C::TMEM_COLS);
@@ -714,6 +718,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
+  auto col_sbuf = [](uint32_t j) { return (j & 1u) ? C::COL_SB1 : C::COL_SB0; };
 
   if (warp == BWD_WARP_LOAD) {
     // ------------------------------------------------------- TMA producer
@@ -724,23 +729,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         QUnit U;
         const int st = q_unit(i, P, U);
         if (st == 0) break;
-        if (st == 1 || U.nmax == 0) continue;
+        if (st == 1 || U.n == 0) continue;
         if (!bwd_wait(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
-        const int nqt = (U.n[0] > 0) + (U.n[1] > 0);
-        mbar_arrive_expect_tx(BAR_Q_FULL, nqt * 2 * C::TILE128);
+        mbar_arrive_expect_tx(BAR_Q_FULL, 2 * C::TILE);
 #pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          if (U.n[t] == 0) continue;
-#pragma unroll
-          for (int c = 0; c < C::NCHUNK; ++c) {
-            tma_load_4d(sbase + C::Q_OFF_Q + t * C::TILE128 + c * C::CH128, &tm_q, BAR_Q_FULL,
-                        c * C::CHUNK_ELEMS, U.hq, U.row0 + t * BWD_TILE, U.b);
-            tma_load_4d(sbase + C::Q_OFF_DO + t * C::TILE128 + c * C::CH128, &tm_do,
-                        BAR_Q_FULL, c * C::CHUNK_ELEMS, U.hq, U.row0 + t * BWD_TILE, U.b);
-          }
+        for (int c = 0; c < C::NCHUNK; ++c) {
+          tma_load_4d(sbase + C::Q_OFF_Q + c * C::CH, &tm_q, BAR_Q_FULL, c * C::CHUNK_ELEMS,
+                      U.hq, U.row0, U.b);
+          tma_load_4d(sbase + C::Q_OFF_DO + c * C::CH, &tm_do, BAR_Q_FULL, c * C::CHUNK_ELEMS,
+                      U.hq, U.row0, U.b);
         }
         ++qit;
-        for (int j = 0; ok && j < U.nmax; ++j) {
+        for (int j = 0; ok && j < U.n; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
             const uint32_t slot = it % C::NSLOT;
@@ -748,12 +748,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(BAR_KV_FULL + 8 * slot, C::TILE64);
+            mbar_arrive_expect_tx(BAR_KV_FULL + 8 * slot, C::TILE);
 #pragma unroll
             for (int c = 0; c < C::NCHUNK; ++c)
-              tma_load_4d(sbase + C::Q_OFF_KV + slot * C::TILE64 + c * C::CH64,
-                          kv ? &tm_v64 : &tm_k64, BAR_KV_FULL + 8 * slot, c * C::CHUNK_ELEMS,
-                          U.hkv, j * BWD_KV_ROWS, U.b);
+              tma_load_4d(sbase + C::Q_OFF_KV + slot * C::TILE + c * C::CH, kv ? &tm_v : &tm_k,
+                          BAR_KV_FULL + 8 * slot, c * C::CHUNK_ELEMS, U.hkv, j * BWD_TILE, U.b);
             ++it;
           }
         }
@@ -765,68 +764,74 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncwarp();
   } else if (warp == BWD_WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    // Per 64-key K/V tile j and Q tile t:
-    //   S_t = Q_t K_j^T, dP_t = dO_t V_j^T  -> sd_full[t]
-    //   (element-wise: dS_t into TMEM)     <- e_full[t]
-    //   dQ_t += dS_t K_j
-    // issued as  SD_0(0) SD_1(0) | DQ_0(0) SD_0(1) | DQ_1(0) SD_1(1) | ...
-    // K_j is released after both DQ(j), V_j after both SD(j).
+    // Per 128-key K/V tile j (S in buffer j & 1):
+    //   S(j) = Q K_j^T -> s_full[j & 1] (issued two tiles ahead)
+    //   dP(j) = dO V_j^T -> dp_full
+    //   <- ds_full (both warpgroups wrote dS(j)):  dQ += dS(j) K_j
+    // issued as  S(0) dP(0) S(1) | dQ(0) dP(1) S(2) | dQ(1) dP(2) S(3) | ...
+    // so the element-wise warps form P(j+1) while dQ(j) runs and dS(j+1)
+    // while S(j+2) runs. In-order execution puts S(j+2) after dQ(j), which
+    // reads dS(j) from the same buffer, and dP(j+1) after the element-wise
+    // warps read dP(j) (ds_full). K_j is released after dQ(j), V_j after dP(j).
     if (lane == 0) {
-      uint32_t it = 0, qit = 0, e[2] = {0u, 0u};
+      uint32_t it = 0, qit = 0, dsc = 0;
       bool ok = true;
-      const uint32_t kv_s = sbase + C::Q_OFF_KV;
-      auto slot_smem = [&](uint32_t f) { return kv_s + (f % C::NSLOT) * C::TILE64; };
+      const uint32_t q_s = sbase + C::Q_OFF_Q, do_s = sbase + C::Q_OFF_DO;
+      auto slot_smem = [&](uint32_t f) { return sbase + C::Q_OFF_KV + (f % C::NSLOT) * C::TILE; };
       auto wait_fill = [&](uint32_t f) {
         return bwd_wait(BAR_KV_FULL + 8 * (f % C::NSLOT), (f / C::NSLOT) & 1u, ctl, P);
-      };
-      auto issue_sd = [&](int t, uint32_t fk) {
-        issue_n64<D, F16>(tmem + 128 * t, sbase + C::Q_OFF_Q + t * C::TILE128, slot_smem(fk),
-                          C::CH64, 0);
-        issue_n64<D, F16>(tmem + 128 * t + 64, sbase + C::Q_OFF_DO + t * C::TILE128,
-                          slot_smem(fk + 1), C::CH64, 0);
-        tc_commit(BAR_SD_FULL + 8 * t);
       };
       for (int i = 0; ok; ++i) {
         QUnit U;
         const int st = q_unit(i, P, U);
         if (st == 0) break;
-        if (st == 1 || U.nmax == 0) continue;
-        if (!bwd_wait(BAR_Q_FULL, qit & 1u, ctl, P)) { ok = false; break; }
-        if (!wait_fill(it) || !wait_fill(it + 1)) { ok = false; break; }
+        if (st == 1 || U.n == 0) continue;
+        const int n = U.n;
+        if (!bwd_wait(BAR_Q_FULL, qit & 1u, ctl, P) || !wait_fill(it) || !wait_fill(it + 1)) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
-#pragma unroll
-        for (int t = 0; t < 2; ++t)
-          if (U.n[t] > 0) issue_sd(t, it);
+        issue_s128<D, F16>(tmem + C::COL_SB0, q_s, slot_smem(it));
+        tc_commit(BAR_S_FULL);
+        issue_s128<D, F16>(tmem + C::COL_DP, do_s, slot_smem(it + 1));
+        tc_commit(BAR_DP_FULL);
         tc_commit(BAR_KV_EMPTY + 8 * ((it + 1) % C::NSLOT));  // V_0
-        if (U.nmax == 1) tc_commit(BAR_Q_EMPTY);
-        for (int j = 0; j < U.nmax; ++j) {
-          const uint32_t fk = it + 2 * j;  // fill of K_j
-          const bool more = j + 1 < U.nmax;
+        if (n == 1) tc_commit(BAR_Q_EMPTY);
+        if (n > 1) {
+          if (!wait_fill(it + 2)) { ok = false; break; }
+          tc_fence_after();
+          issue_s128<D, F16>(tmem + C::COL_SB1, q_s, slot_smem(it + 2));
+          tc_commit(BAR_S_FULL + 8);
+        }
+        for (int j = 0; j < n; ++j) {
+          const uint32_t fk = it + 2 * j;  // fill of K_j; V_j is fk + 1
+          if (!bwd_wait(BAR_DS_FULL, dsc & 1u, ctl, P)) { ok = false; break; }
+          ++dsc;
+          tc_fence_after();
 #pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j < U.n[t]) {
-              if (!bwd_wait(BAR_E_FULL + 8 * t, e[t] & 1u, ctl, P)) { ok = false; break; }
-              ++e[t];
-              tc_fence_after();
-              issue_acc64<D, F16>(tmem + C::COL_DQ + t * D, tmem + 128 * t, slot_smem(fk),
-                                  C::CH64, 0, j > 0);
-              if (j == U.n[t] - 1) tc_commit(BAR_DQ_FULL + 8 * t);
-            }
-            if (t == 0 && more) {
-              if (!wait_fill(fk + 2) || !wait_fill(fk + 3)) { ok = false; break; }
-              tc_fence_after();
-            }
-            if (j + 1 < U.n[t]) issue_sd(t, fk + 2);
-          }
-          if (!ok) break;
+          for (int h = 0; h < 2; ++h)
+            issue_acc64<D, F16>(tmem + C::COL_DQ, tmem + col_sbuf(j) + BWD_HALF * h,
+                                slot_smem(fk), C::CH, BWD_HALF * h, j > 0 || h > 0);
           tc_commit(BAR_KV_EMPTY + 8 * (fk % C::NSLOT));  // K_j
-          if (more) {
+          if (j + 1 < n) {
+            if (!wait_fill(fk + 3)) { ok = false; break; }
+            tc_fence_after();
+            issue_s128<D, F16>(tmem + C::COL_DP, do_s, slot_smem(fk + 3));
+            tc_commit(BAR_DP_FULL);
             tc_commit(BAR_KV_EMPTY + 8 * ((fk + 3) % C::NSLOT));  // V_{j+1}
-            if (j + 2 == U.nmax) tc_commit(BAR_Q_EMPTY);
+            if (j + 2 == n) tc_commit(BAR_Q_EMPTY);  // dP(n-1) is the last reader of Q / dO
+          }
+          if (j + 2 < n) {
+            if (!wait_fill(fk + 4)) { ok = false; break; }
+            tc_fence_after();
+            issue_s128<D, F16>(tmem + col_sbuf(j), q_s, slot_smem(fk + 4));
+            tc_commit(BAR_S_FULL + 8 * (j & 1));
           }
         }
         if (!ok) break;
-        it += 2 * U.nmax;
+        tc_commit(BAR_DQ_FULL);
+        it += 2 * n;
         ++qit;
       }
       tc_commit(BAR_DRAIN);
@@ -835,82 +840,94 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------ element-wise
-    // Thread = one query row of Q tile t (TMEM lane).
-    const int t = warp >> 2;
+    // Thread = one query row of the unit (TMEM lane); warpgroup h = keys
+    // [64 h, 64 h + 64) of each K/V tile, and columns [h d/2, h d/2 + d/2)
+    // of the row's dQ in the epilogue.
+    const int h = warp >> 2;
     const int quad = warp & 3;
     const int rloc = quad * 32 + lane;
     const uint32_t t_lane = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    const uint32_t col_s = 128 * t, col_dp = 128 * t + 64, col_dq = C::COL_DQ + t * D;
+    const uint32_t col_dp = C::COL_DP + BWD_HALF * h;
     const float cs = P.scale_log2;
-    uint32_t sd = 0, dqc = 0;
+    uint32_t sfc[2] = {0u, 0u}, dpc = 0, dqc = 0;
     bool ok = true;
     for (int i = 0; ok; ++i) {
       QUnit U;
       const int st = q_unit(i, P, U);
       if (st == 0) break;
       if (st == 1) continue;
-      const int tile_row0 = U.row0 + t * BWD_TILE;
-      if (tile_row0 >= P.Sq) continue;
-      const int row = tile_row0 + rloc;  // < Sq_pad
+      const int row = U.row0 + rloc;  // < Sq_pad
       const bool row_ok = row < P.Sq;
-      const int n = U.n[t];
       const size_t ridx = (static_cast<size_t>(U.b) * P.Hq + U.hq) * P.Sq_pad + row;
       const float l2 = P.lse2[ridx];
       const float dsr = P.dsum[ridx];
-      for (int j = 0; j < n; ++j) {
-        const bool w = bwd_wait(BAR_SD_FULL + 8 * t, sd & 1u, ctl, P);
-        ++sd;
+      for (int j = 0; j < U.n; ++j) {
+        const uint32_t buf = j & 1;
+        bool w = bwd_wait(BAR_S_FULL + 8 * buf, sfc[buf] & 1u, ctl, P);
+        ++sfc[buf];
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sr[64], dr[64];
+        const uint32_t col_s = col_sbuf(j) + BWD_HALF * h;
+        // keys key0 + c, c >= vis, are masked (past Sk, or after row + Sk - Sq)
+        const int key0 = j * BWD_TILE + BWD_HALF * h;
+        int vis = P.Sk - key0;
+        if (P.causal) vis = min(vis, row + (P.Sk - P.Sq) - key0 + 1);
+        float p[64];
         {
+          uint32_t sr[64];
           uint32_t (&s0)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr);
           uint32_t (&s1)[32] = *reinterpret_cast<uint32_t(*)[32]>(sr + 32);
-          uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr);
-          uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr + 32);
           tmem_ld32_async(t_lane + col_s, s0);
           tmem_ld32_async(t_lane + col_s + 32, s1);
-          tmem_ld32_async(t_lane + col_dp, d0);
-          tmem_ld32_async(t_lane + col_dp + 32, d1);
           tmem_ld_wait();
           reg_fence(s0);
           reg_fence(s1);
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -l2));
+            p[c] = c < vis ? x : 0.f;
+          }
+        }
+        w = bwd_wait(BAR_DP_FULL, dpc & 1u, ctl, P);
+        ++dpc;
+        if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
+        tc_fence_after();
+        {
+          uint32_t dr[64];
+          uint32_t (&d0)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr);
+          uint32_t (&d1)[32] = *reinterpret_cast<uint32_t(*)[32]>(dr + 32);
+          tmem_ld32_async(t_lane + col_dp, d0);
+          tmem_ld32_async(t_lane + col_dp + 32, d1);
+          tmem_ld_wait();
           reg_fence(d0);
           reg_fence(d1);
-        }
-        // keys key0 + c, c >= vis, are masked (past Sk, or after row + Sk - Sq)
-        const int key0 = j * BWD_KV_ROWS;
-        int vis = P.Sk - key0;
-        if (P.causal) vis = min(vis, row + (P.Sk - P.Sq) - key0 + 1);
-        uint32_t pk[32];
+          uint32_t pk[32];
 #pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -l2));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + 1]), cs, -l2));
-          p0 = c < vis ? p0 : 0.f;
-          p1 = c + 1 < vis ? p1 : 0.f;
-          pk[c / 2] = pack16x2(F16, p0 * (__uint_as_float(dr[c]) - dsr),
-                               p1 * (__uint_as_float(dr[c + 1]) - dsr));
+          for (int c = 0; c < 64; c += 2)
+            pk[c / 2] = pack16x2(F16, p[c] * (__uint_as_float(dr[c]) - dsr),
+                                 p[c + 1] * (__uint_as_float(dr[c + 1]) - dsr));
+          tmem_st32(t_lane + col_s, pk);
+          tmem_st_wait();
         }
-        tmem_st32(t_lane + col_s, pk);
-        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(BAR_E_FULL + 8 * t);
+        if (lane == 0) mbar_arrive(BAR_DS_FULL);
       }
       if (!ok) break;
       // ------------------------------------------------------ epilogue
-      uint16_t* out = P.dq + ((static_cast<size_t>(U.b) * P.Sq + row) * P.Hq + U.hq) *
-                                 static_cast<size_t>(D);
-      if (n > 0) {
-        const bool w = bwd_wait(BAR_DQ_FULL + 8 * t, dqc & 1u, ctl, P);
+      constexpr int HALF_D = D / 2;
+      uint16_t* out = P.dq +
+                      ((static_cast<size_t>(U.b) * P.Sq + row) * P.Hq + U.hq) *
+                          static_cast<size_t>(D) + HALF_D * h;
+      if (U.n > 0) {
+        const bool w = bwd_wait(BAR_DQ_FULL, dqc & 1u, ctl, P);
         ++dqc;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
+        for (int q = 0; q < HALF_D / 32; ++q) {
           uint32_t r[32];
-          tmem_ld32(t_lane + col_dq + 32 * q, r);
+          tmem_ld32(t_lane + C::COL_DQ + HALF_D * h + 32 * q, r);
           uint32_t pk[16];
 #pragma unroll
           for (int c = 0; c < 16; ++c)
@@ -923,10 +940,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
               dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
           }
         }
+        tc_fence_before();
       } else if (row_ok) {
         uint4* dst = reinterpret_cast<uint4*>(out);
 #pragma unroll
-        for (int v = 0; v < D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+        for (int v = 0; v < HALF_D / 8; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
       }
     }
   }
