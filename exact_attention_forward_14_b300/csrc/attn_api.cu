@@ -261,8 +261,8 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   P.dq = static_cast<uint16_t*>(dq);
   P.dk = static_cast<uint16_t*>(dk);
   P.dv = static_cast<uint16_t*>(dv);
-  P.lse2 = ws;
-  P.dsum = ws + rows_pad;
+  P.nlse2 = ws;
+  P.ndsum = ws + rows_pad;
   P.B = B;
   P.Hq = Hq;
   P.Hkv = Hkv;

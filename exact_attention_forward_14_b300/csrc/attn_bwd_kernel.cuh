@@ -60,8 +60,8 @@ struct BwdParams {
   uint16_t* dq;         // [B, Sq, Hq, d]
   uint16_t* dk;         // [B, Sk, Hkv, d]
   uint16_t* dv;         // [B, Sk, Hkv, d]
-  const float* lse2;    // [B, Hq, Sq_pad]: LSE * log2(e); +inf past Sq and for rows without keys
-  const float* dsum;    // [B, Hq, Sq_pad]: D = rowsum(dO * O); 0 past Sq
+  const float* nlse2;   // [B, Hq, Sq_pad]: -LSE * log2(e); -inf past Sq and for rows without keys
+  const float* ndsum;   // [B, Hq, Sq_pad]: -D = -rowsum(dO * O); 0 past Sq
   int B, Hq, Hkv, Sq, Sk, Sq_pad;
   int group;            // Hq / Hkv
   int causal;
@@ -90,7 +90,7 @@ struct BwdCfg {
   static constexpr uint32_t IDESC_ACC = make_idesc(128, D, FMT, true);   // dV, dK, dQ
   static constexpr int TMEM_COLS = 512;
   static constexpr int SMEM_ALLOC = 227 * 1024;
-  // ---- dK/dV kernel: K, V, then NSTAGE stages of (Q, dO, lse2[128], D[128])
+  // ---- dK/dV kernel: K, V, then NSTAGE stages of (Q, dO, -lse2[128], -D[128])
   static constexpr int NSTAGE = D == 128 ? 2 : 4;
   static constexpr int STAGE = 2 * TILE + 1024;
   static constexpr int KV_OFF_K = 0;
@@ -174,6 +174,13 @@ __device__ __forceinline__ void bwd_drain_wait(uint32_t bar, uint32_t parity, co
   }
 }
 
+// Lane-wise a * b on fp32 pairs (round to nearest even).
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __device__ __forceinline__ uint32_t pack16x2(bool f16, float lo, float hi) {
   return f16 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi);
 }
@@ -212,14 +219,16 @@ __device__ __forceinline__ void issue_acc64(uint32_t d_tmem, uint32_t a_tmem, ui
 
 // ------------------------------------------------------------------ prep --
 
-// D[r] = sum_c dO[r, c] * O[r, c] (fp32) and lse2[r] = LSE[r] * log2(e) for
+// -D[r] = -sum_c dO[r, c] * O[r, c] (fp32) and -lse2[r] = -LSE[r] * log2(e) for
 // every padded row r = (b Hq + hq) Sq_pad + i; rows i >= Sq (and rows whose
-// LSE is -inf, i.e. that see no key) get lse2 = +inf, which zeroes their P.
+// LSE is -inf, i.e. that see no key) get -lse2 = -inf, which zeroes their P.
+// (Stored negated so that the exponent s * c - lse2 and dP - D are one fused
+// add each.)
 template <int D, bool F16>
 __global__ void __launch_bounds__(BWD_PREP_THREADS)
     bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
-                    const float* __restrict__ lse, float* __restrict__ lse2,
-                    float* __restrict__ dsum, int Hq, int Sq, int Sq_pad, long long rows_pad) {
+                    const float* __restrict__ lse, float* __restrict__ nlse2,
+                    float* __restrict__ ndsum, int Hq, int Sq, int Sq_pad, long long rows_pad) {
   constexpr int PER = D / 32;  // elements per lane
   const long long r =
       static_cast<long long>(blockIdx.x) * (BWD_PREP_THREADS / 32) + (threadIdx.x >> 5);
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(BWD_PREP_THREADS)
   const int lane = threadIdx.x & 31;
   const long long bh = r / Sq_pad;
   const int i = static_cast<int>(r - bh * Sq_pad);
-  float acc = 0.f, l2 = INFINITY;
+  float acc = 0.f, l2 = -INFINITY;
   if (i < Sq) {
     const long long b = bh / Hq, hq = bh - b * Hq;
     const size_t off = ((static_cast<size_t>(b) * Sq + i) * Hq + hq) * D + lane * PER;
@@ -260,11 +269,11 @@ __global__ void __launch_bounds__(BWD_PREP_THREADS)
 #pragma unroll
     for (int off2 = 16; off2 > 0; off2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off2);
     const float L = lse[bh * Sq + i];
-    l2 = (L == -INFINITY) ? INFINITY : L * BWD_LOG2E;
+    l2 = (L == -INFINITY) ? -INFINITY : -L * BWD_LOG2E;
   }
   if (lane == 0) {
-    lse2[r] = l2;
-    dsum[r] = acc;
+    nlse2[r] = l2;
+    ndsum[r] = -acc;
   }
 }
 
@@ -401,8 +410,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           }
           const size_t row = (static_cast<size_t>(U.b) * P.Hq + hq) * P.Sq_pad +
                              static_cast<size_t>(qi) * BWD_TILE;
-          bulk_load(stg + 2 * C::TILE, P.lse2 + row, 512, bar);
-          bulk_load(stg + 2 * C::TILE + 512, P.dsum + row, 512, bar);
+          bulk_load(stg + 2 * C::TILE, P.nlse2 + row, 512, bar);
+          bulk_load(stg + 2 * C::TILE + 512, P.ndsum + row, 512, bar);
           ++n;
         }
       }
@@ -517,7 +526,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t nn = n + t;
         bool w = bwd_wait(BAR_S_FULL, sc & 1u, ctl, P);
         ++sc;
-        // lse2 / D of this tile were staged by TMA on st_full (already
+        // -lse2 / -D of this tile were staged by TMA on st_full (already
         // complete: the MMA waited for it before issuing S^T)
         w = w && bwd_wait(BAR_ST_FULL + 8 * (nn % C::NSTAGE), (nn / C::NSTAGE) & 1u, ctl, P);
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -541,21 +550,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld_wait();
           reg_fence(s0);
           reg_fence(s1);
-          uint32_t pk[32];
+          // p = 2^(s c - lse2): paired fp32 FMA, one MUFU ex2 per score
+          const uint64_t cs2 = f2_pack(cs, cs);
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const uint4 l4 = lds128(lse_s + 16 * c4);
-            const float lv[4] = {__uint_as_float(l4.x), __uint_as_float(l4.y),
-                                 __uint_as_float(l4.z), __uint_as_float(l4.w)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -lv[e]));
-              p[c] = c < cmin ? 0.f : x;
-            }
-            pk[2 * c4] = pack16x2(F16, p[4 * c4], p[4 * c4 + 1]);
-            pk[2 * c4 + 1] = pack16x2(F16, p[4 * c4 + 2], p[4 * c4 + 3]);
+            float x0, x1, x2, x3;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * c4]), __uint_as_float(sr[4 * c4 + 1])),
+                             cs2, f2_pack(__uint_as_float(l4.x), __uint_as_float(l4.y))), x0, x1);
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[4 * c4 + 2]), __uint_as_float(sr[4 * c4 + 3])),
+                             cs2, f2_pack(__uint_as_float(l4.z), __uint_as_float(l4.w))), x2, x3);
+            p[4 * c4] = ex2_approx(x0);
+            p[4 * c4 + 1] = ex2_approx(x1);
+            p[4 * c4 + 2] = ex2_approx(x2);
+            p[4 * c4 + 3] = ex2_approx(x3);
           }
+          if (__any_sync(0xffffffffu, cmin > 0)) {  // diagonal tiles and keys past Sk
+#pragma unroll
+            for (int c = 0; c < 64; ++c) p[c] = c < cmin ? 0.f : p[c];
+          }
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack16x2(F16, p[2 * c], p[2 * c + 1]);
           tmem_st32(t_lane + col_s, pk);
           tmem_st_wait();
         }
@@ -576,20 +592,22 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           tmem_ld_wait();
           reg_fence(d0);
           reg_fence(d1);
+          // dS = P (dP - D), on fp32 pairs
           uint32_t pd[32];
 #pragma unroll
           for (int c4 = 0; c4 < 16; ++c4) {
             const uint4 d4 = lds128(dsum_s + 16 * c4);
-            const float dv4[4] = {__uint_as_float(d4.x), __uint_as_float(d4.y),
-                                  __uint_as_float(d4.z), __uint_as_float(d4.w)};
-            float ds[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c = 4 * c4 + e;
-              ds[e] = p[c] * (__uint_as_float(dr[c]) - dv4[e]);
-            }
-            pd[2 * c4] = pack16x2(F16, ds[0], ds[1]);
-            pd[2 * c4 + 1] = pack16x2(F16, ds[2], ds[3]);
+            float y0, y1, y2, y3;
+            f2_unpack(f2_mul(f2_pack(p[4 * c4], p[4 * c4 + 1]),
+                             f2_add(f2_pack(__uint_as_float(dr[4 * c4]), __uint_as_float(dr[4 * c4 + 1])),
+                                    f2_pack(__uint_as_float(d4.x), __uint_as_float(d4.y)))),
+                      y0, y1);
+            f2_unpack(f2_mul(f2_pack(p[4 * c4 + 2], p[4 * c4 + 3]),
+                             f2_add(f2_pack(__uint_as_float(dr[4 * c4 + 2]), __uint_as_float(dr[4 * c4 + 3])),
+                                    f2_pack(__uint_as_float(d4.z), __uint_as_float(d4.w)))),
+                      y2, y3);
+            pd[2 * c4] = pack16x2(F16, y0, y1);
+            pd[2 * c4 + 1] = pack16x2(F16, y2, y3);
           }
           tmem_st32(t_lane + col_dp, pd);
           tmem_st_wait();
@@ -859,8 +877,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
       const int row = U.row0 + rloc;  // < Sq_pad
       const bool row_ok = row < P.Sq;
       const size_t ridx = (static_cast<size_t>(U.b) * P.Hq + U.hq) * P.Sq_pad + row;
-      const float l2 = P.lse2[ridx];
-      const float dsr = P.dsum[ridx];
+      const float nl2 = P.nlse2[ridx];
+      const float nds = P.ndsum[ridx];
+      const uint64_t cs2 = f2_pack(cs, cs), nl22 = f2_pack(nl2, nl2), nds2 = f2_pack(nds, nds);
       for (int j = 0; j < U.n; ++j) {
         const uint32_t buf = j & 1;
         bool w = bwd_wait(BAR_S_FULL + 8 * buf, sfc[buf] & 1u, ctl, P);
@@ -883,9 +902,16 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           reg_fence(s0);
           reg_fence(s1);
 #pragma unroll
-          for (int c = 0; c < 64; ++c) {
-            const float x = ex2_approx(fmaf(__uint_as_float(sr[c]), cs, -l2));
-            p[c] = c < vis ? x : 0.f;
+          for (int c = 0; c < 64; c += 2) {
+            float x0, x1;
+            f2_unpack(f2_fma(f2_pack(__uint_as_float(sr[c]), __uint_as_float(sr[c + 1])), cs2,
+                             nl22), x0, x1);
+            p[c] = ex2_approx(x0);
+            p[c + 1] = ex2_approx(x1);
+          }
+          if (__any_sync(0xffffffffu, vis < BWD_HALF)) {  // diagonal tiles and keys past Sk
+#pragma unroll
+            for (int c = 0; c < 64; ++c) p[c] = c < vis ? p[c] : 0.f;
           }
         }
         w = bwd_wait(BAR_DP_FULL, dpc & 1u, ctl, P);
@@ -903,9 +929,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
           reg_fence(d1);
           uint32_t pk[32];
 #pragma unroll
-          for (int c = 0; c < 64; c += 2)
-            pk[c / 2] = pack16x2(F16, p[c] * (__uint_as_float(dr[c]) - dsr),
-                                 p[c + 1] * (__uint_as_float(dr[c + 1]) - dsr));
+          for (int c = 0; c < 64; c += 2) {
+            float y0, y1;
+            f2_unpack(f2_mul(f2_pack(p[c], p[c + 1]),
+                             f2_add(f2_pack(__uint_as_float(dr[c]), __uint_as_float(dr[c + 1])),
+                                    nds2)),
+                      y0, y1);
+            pk[c / 2] = pack16x2(F16, y0, y1);
+          }
           tmem_st32(t_lane + col_s, pk);
           tmem_st_wait();
         }
