@@ -282,12 +282,19 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   P.timeout_ns = kWaitLimitNs;
   P.status = di->status;
 
+  // row statistics: warps over the rows in memory order (D / 8 lanes per row,
+  // BWD_PREP_STEPS row groups per warp), then one thread per padded entry
+  const long long rows = static_cast<long long>(B) * Sq * Hq;
+  const long long rows_per_warp = (32 / (D / 8)) * attnb3::BWD_PREP_STEPS;
+  const long long row_warps = (rows + rows_per_warp - 1) / rows_per_warp;
+  const long long pad_rows = static_cast<long long>(B) * Hq * (P.Sq_pad - Sq);
+  const long long warps = row_warps + (pad_rows + 31) / 32;
   const long long per_block = attnb3::BWD_PREP_THREADS / 32;
-  const long long prep_blocks = (rows_pad + per_block - 1) / per_block;
+  const long long prep_blocks = (warps + per_block - 1) / per_block;
   attnb3::bwd_prep_kernel<D, F16><<<static_cast<unsigned>(prep_blocks),
                                     attnb3::BWD_PREP_THREADS, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, ws,
-      ws + rows_pad, Hq, Sq, P.Sq_pad, rows_pad);
+      ws + rows_pad, Hq, Sq, P.Sq_pad, rows, row_warps, pad_rows);
   const int gkv = P.kv_items < di->num_sms ? P.kv_items : di->num_sms;
   kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
   const int gq = P.q_items < di->num_sms ? P.q_items : di->num_sms;

@@ -11,8 +11,8 @@
 // (GQA: the query heads sharing a KV head sum into its dK and dV.)
 //
 // Three launches:
-//   bwd_prep_kernel  D and LSE * log2(e) per query row, padded to whole
-//                    128-row tiles (HBM-bound, one warp per row);
+//   bwd_prep_kernel  -D and -LSE * log2(e) per query row, padded to whole
+//                    128-row tiles (HBM-bound: O and dO read once);
 //   bwd_dkdv_kernel  unit = (b, KV head, 128 keys): K and V stay in shared
 //                    memory while the Q / dO tiles of every query head of the
 //                    group stream past; dK and dV accumulate in tensor memory
@@ -219,61 +219,81 @@ __device__ __forceinline__ void issue_acc64(uint32_t d_tmem, uint32_t a_tmem, ui
 
 // ------------------------------------------------------------------ prep --
 
-// -D[r] = -sum_c dO[r, c] * O[r, c] (fp32) and -lse2[r] = -LSE[r] * log2(e) for
-// every padded row r = (b Hq + hq) Sq_pad + i; rows i >= Sq (and rows whose
-// LSE is -inf, i.e. that see no key) get -lse2 = -inf, which zeroes their P.
-// (Stored negated so that the exponent s * c - lse2 and dP - D are one fused
-// add each.)
+// -D = -sum_c dO[r, c] * O[r, c] (fp32) and -lse2 = -LSE * log2(e) for every
+// query row, stored at (b Hq + hq) Sq_pad + i; the padded entries i >= Sq
+// (and rows whose LSE is -inf, i.e. that see no key) get -lse2 = -inf, which
+// zeroes their P. (Stored negated so that the exponent s * c - lse2 and
+// dP - D are one fused add each.)
+// HBM-bound: rows are read in memory order ([B, Sq, Hq] with d contiguous),
+// d / 8 lanes per row with 16-byte loads, two row groups in flight per warp.
+// Warps past the rows write the padded entries.
+constexpr int BWD_PREP_STEPS = 2;
+
 template <int D, bool F16>
 __global__ void __launch_bounds__(BWD_PREP_THREADS)
     bwd_prep_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ d_o,
                     const float* __restrict__ lse, float* __restrict__ nlse2,
-                    float* __restrict__ ndsum, int Hq, int Sq, int Sq_pad, long long rows_pad) {
-  constexpr int PER = D / 32;  // elements per lane
-  const long long r =
-      static_cast<long long>(blockIdx.x) * (BWD_PREP_THREADS / 32) + (threadIdx.x >> 5);
-  if (r >= rows_pad) return;
+                    float* __restrict__ ndsum, int Hq, int Sq, int Sq_pad, long long rows,
+                    long long row_warps, long long pad_rows) {
+  constexpr int LPR = D / 8;     // lanes per row
+  constexpr int RPW = 32 / LPR;  // rows per warp per step
   const int lane = threadIdx.x & 31;
-  const long long bh = r / Sq_pad;
-  const int i = static_cast<int>(r - bh * Sq_pad);
-  float acc = 0.f, l2 = -INFINITY;
-  if (i < Sq) {
-    const long long b = bh / Hq, hq = bh - b * Hq;
-    const size_t off = ((static_cast<size_t>(b) * Sq + i) * Hq + hq) * D + lane * PER;
-    uint32_t ow[PER / 2], gw[PER / 2];
-    if constexpr (PER == 4) {
-      const uint2 a = *reinterpret_cast<const uint2*>(o + off);
-      const uint2 g = *reinterpret_cast<const uint2*>(d_o + off);
-      ow[0] = a.x; ow[1] = a.y; gw[0] = g.x; gw[1] = g.y;
-    } else {
-      ow[0] = *reinterpret_cast<const uint32_t*>(o + off);
-      gw[0] = *reinterpret_cast<const uint32_t*>(d_o + off);
+  const long long gw =
+      (static_cast<long long>(blockIdx.x) * BWD_PREP_THREADS + threadIdx.x) >> 5;
+  if (gw >= row_warps) {  // padded entries, one per thread
+    const long long k = (gw - row_warps) * 32 + lane;
+    const int pad = Sq_pad - Sq;
+    if (k < pad_rows) {
+      const long long idx = (k / pad) * Sq_pad + Sq + k % pad;
+      nlse2[idx] = -INFINITY;
+      ndsum[idx] = 0.f;
     }
+    return;
+  }
+  const int sub = lane / LPR, part = lane % LPR;
+  uint4 a[BWD_PREP_STEPS], g[BWD_PREP_STEPS];
+  long long rr[BWD_PREP_STEPS];
 #pragma unroll
-    for (int e = 0; e < PER / 2; ++e) {
+  for (int s = 0; s < BWD_PREP_STEPS; ++s) {
+    rr[s] = (gw * BWD_PREP_STEPS + s) * RPW + sub;
+    a[s] = g[s] = make_uint4(0u, 0u, 0u, 0u);
+    if (rr[s] < rows) {
+      a[s] = *reinterpret_cast<const uint4*>(o + rr[s] * D + part * 8);
+      g[s] = *reinterpret_cast<const uint4*>(d_o + rr[s] * D + part * 8);
+    }
+  }
+#pragma unroll
+  for (int s = 0; s < BWD_PREP_STEPS; ++s) {
+    const uint32_t aw[4] = {a[s].x, a[s].y, a[s].z, a[s].w};
+    const uint32_t gw4[4] = {g[s].x, g[s].y, g[s].z, g[s].w};
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
       float a0, a1, g0, g1;
       if constexpr (F16) {
-        a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(ow[e] & 0xFFFFu)));
-        a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(ow[e] >> 16)));
-        g0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gw[e] & 0xFFFFu)));
-        g1 = __half2float(__ushort_as_half(static_cast<unsigned short>(gw[e] >> 16)));
+        a0 = __half2float(__ushort_as_half(static_cast<unsigned short>(aw[e] & 0xFFFFu)));
+        a1 = __half2float(__ushort_as_half(static_cast<unsigned short>(aw[e] >> 16)));
+        g0 = __half2float(__ushort_as_half(static_cast<unsigned short>(gw4[e] & 0xFFFFu)));
+        g1 = __half2float(__ushort_as_half(static_cast<unsigned short>(gw4[e] >> 16)));
       } else {
-        a0 = __uint_as_float(ow[e] << 16);
-        a1 = __uint_as_float(ow[e] & 0xFFFF0000u);
-        g0 = __uint_as_float(gw[e] << 16);
-        g1 = __uint_as_float(gw[e] & 0xFFFF0000u);
+        a0 = __uint_as_float(aw[e] << 16);
+        a1 = __uint_as_float(aw[e] & 0xFFFF0000u);
+        g0 = __uint_as_float(gw4[e] << 16);
+        g1 = __uint_as_float(gw4[e] & 0xFFFF0000u);
       }
       acc = fmaf(a0, g0, acc);
       acc = fmaf(a1, g1, acc);
     }
 #pragma unroll
-    for (int off2 = 16; off2 > 0; off2 >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off2);
-    const float L = lse[bh * Sq + i];
-    l2 = (L == -INFINITY) ? -INFINITY : -L * BWD_LOG2E;
-  }
-  if (lane == 0) {
-    nlse2[r] = l2;
-    ndsum[r] = -acc;
+    for (int off = LPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (part == 0 && rr[s] < rows) {
+      const long long hq = rr[s] % Hq, bi = rr[s] / Hq;  // rr = (b Sq + i) Hq + hq
+      const long long i = bi % Sq, b = bi / Sq;
+      const long long bh = b * Hq + hq;
+      const float L = lse[bh * Sq + i];
+      nlse2[bh * Sq_pad + i] = (L == -INFINITY) ? -INFINITY : -L * BWD_LOG2E;
+      ndsum[bh * Sq_pad + i] = -acc;
+    }
   }
 }
 
