@@ -45,12 +45,14 @@ DEFAULT_WORKLOAD = "b2h32s8192d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
                   "exact_attention_forward_14_b300/csrc/ptx.cuh"]
+KERNEL_SOURCES_BWD = ["exact_attention_forward_14_b300/csrc/attn_bwd_kernel.cuh",
+                      "exact_attention_forward_14_b300/csrc/ptx.cuh"]
 PROFILES = os.path.join(ROOT, "profiles")
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -64,12 +66,13 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch from the JSON block of a committed ncu summary
-    (profiles/*.md), only while the kernel sources still match the capture."""
+def ncu_traffic(workload: str, sources=KERNEL_SOURCES):
+    """DRAM bytes per launch (per call, for the backward's three kernels) from
+    the JSON block of a committed ncu summary (profiles/*.md), only while the
+    kernel sources still match the capture."""
     import glob
     import re
-    want = kernel_source_hash()
+    want = kernel_source_hash(sources)
     for path in sorted(glob.glob(os.path.join(PROFILES, "*.md"))):
         with open(path) as f:
             text = f.read()
@@ -539,7 +542,8 @@ def run_ours(args, w):
     peak = peaks["bf16_tflops"] * (2.0 if w.dtype == "e4m3" else 1.0)
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-        "frac": achieved / peak, "traffic": ncu_traffic(w.name),
+        "frac": achieved / peak,
+        "traffic": ncu_traffic(w.name, KERNEL_SOURCES_BWD if bwd is not None else KERNEL_SOURCES),
         "kernel": (f"attn_bwd (bwd_prep_kernel + bwd_dkdv_kernel + bwd_dq_kernel)<{w.d},"
                    f"{str(w.dtype == 'f16').lower()}>, executed FLOPs (7 products per pair)"
                    if bwd is not None else
