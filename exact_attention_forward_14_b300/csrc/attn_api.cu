@@ -16,6 +16,7 @@
 
 #include "attn_b300.h"
 #include "attn_bwd_kernel.cuh"
+#include "attn_fwd_d256.cuh"
 #include "attn_fwd_kernel.cuh"
 #include "quantize_fp8.cuh"
 #include "qk_rmsnorm.cuh"
@@ -160,10 +161,55 @@ int check_attn_args(const void* q, const void* k, const void* v, void* o, float*
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
   if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (!fits_i32(B, Sq, Hq, d) || !fits_i32(B, Sk, Hkv, d)) return ATTN_ERR_INVALID_ARG;
-  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (d != 64 && d != 128 && d != 256) return ATTN_ERR_UNSUPPORTED;
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(o, 16) || !aligned(lse, 4))
     return ATTN_ERR_MISALIGNED;
   return ATTN_OK;
+}
+
+// d = 256 forward (bf16 / fp16): one 128-row Q tile per unit, 64-key K/V
+// tiles (attn_fwd_d256.cuh).
+template <bool F16>
+int launch_d256(const void* q, const void* k, const void* v, void* o, float* lse, int B, int Hq,
+                int Hkv, int Sq, int Sk, int causal, float scale, cudaStream_t stream,
+                DeviceInfo* di, uint32_t attr_bit) {
+  using C = attnb3::WideCfg<F16>;
+  auto kern = attnb3::attn_fwd_d256_kernel<F16>;
+  if (!(di->attr_done.load(std::memory_order_acquire) & attr_bit)) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
+        cudaSuccess)
+      return ATTN_ERR_CUDA;
+    di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
+  }
+  CUtensorMap tq, tk, tv;
+  if (!encode_bshd(&tq, q, false, B, Sq, Hq, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::BM, F16) ||
+      !encode_bshd(&tk, k, false, B, Sk, Hkv, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::WIDE_BN,
+                   F16) ||
+      !encode_bshd(&tv, v, false, B, Sk, Hkv, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::WIDE_BN,
+                   F16))
+    return ATTN_ERR_CUDA;
+  FwdParams P{};
+  P.o = static_cast<uint16_t*>(o);
+  P.lse = lse;
+  P.B = B;
+  P.Hq = Hq;
+  P.Hkv = Hkv;
+  P.Sq = Sq;
+  P.Sk = Sk;
+  P.group = Hq / Hkv;
+  P.n_qp = (Sq + attnb3::BM - 1) / attnb3::BM;
+  P.npair = (P.n_qp + 1) / 2;
+  P.nkv = (Sk + attnb3::WIDE_BN - 1) / attnb3::WIDE_BN;
+  P.num_items = B * Hq * P.npair;
+  P.causal = causal ? 1 : 0;
+  P.nsplit = 1;
+  P.kps = P.nkv;
+  P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  P.timeout_ns = kWaitLimitNs;
+  P.status = di->status;
+  const int grid = P.num_items < di->num_sms ? P.num_items : di->num_sms;
+  kern<<<grid, attnb3::WIDE_THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 int run_attn(const void* q, const void* k, const void* v, const float* qs, const float* ks,
@@ -174,6 +220,13 @@ int run_attn(const void* q, const void* k, const void* v, const float* qs, const
   int rc = current_device(&di);
   if (rc != ATTN_OK) return rc;
   if (!get_encoder()) return ATTN_ERR_CUDA;
+  if (d == 256) {  // bf16 / fp16, unsplit only
+    if (fp8 || sp.nsplit != 1 || sp.o_part != nullptr) return ATTN_ERR_UNSUPPORTED;
+    return f16 ? launch_d256<true>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
+                                   di, 1024u)
+               : launch_d256<false>(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, causal, scale, stream,
+                                    di, 2048u);
+  }
   if (fp8 && d == 128)
     return launch<128, true, false>(q, k, v, qs, ks, vs, o, lse, B, Hq, Hkv, Sq, Sk, causal,
                                     scale, stream, di, 4u, sp);
@@ -342,6 +395,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse, i
   if (dtype == ATTN_BF16 || dtype == ATTN_F16)
     return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
                     scale, false, dtype == ATTN_F16, reinterpret_cast<cudaStream_t>(stream));
+  if (dtype == ATTN_FP8_E4M3 && d == 256) return ATTN_ERR_UNSUPPORTED;
   if (dtype == ATTN_FP8_E4M3)  // null scale pointers: every block scale is 1
     return run_attn(q, k, v, nullptr, nullptr, nullptr, o, lse, B, Hq, Hkv, Sq, Sk, d, causal,
                     scale, true, false, reinterpret_cast<cudaStream_t>(stream));
@@ -353,6 +407,7 @@ int attn_fwd_fp8(const void* q, const void* k, const void* v, const float* q_sca
                  int Hkv, int Sq, int Sk, int d, int causal, float scale, attn_stream_t stream) {
   int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
   if (!q_scale || !k_scale || !v_scale) return ATTN_ERR_INVALID_ARG;
   if (!aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
     return ATTN_ERR_MISALIGNED;
@@ -406,6 +461,7 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
   int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
   if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   int kps = 0, nsplit = 0;
   split_shape(Sk, num_splits, &kps, &nsplit);
@@ -434,6 +490,7 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              float scale, int dtype, int num_splits, attn_stream_t stream) {
   int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   int kps = 0, nsplit = 0;
   split_shape(Sk, num_splits, &kps, &nsplit);
@@ -515,6 +572,7 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
   if (rc != ATTN_OK) return rc;
   if (!d_o || !dq || !dk || !dv) return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
+  if (d == 256) return ATTN_ERR_UNSUPPORTED;
   // padded row statistics are indexed with 32-bit row counts
   if (static_cast<long long>(B) * Hq * static_cast<long long>(bwd_sq_pad(Sq)) > 0x7fffffffLL)
     return ATTN_ERR_INVALID_ARG;

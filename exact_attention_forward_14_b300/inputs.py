@@ -83,6 +83,9 @@ WORKLOADS = {
     "bwd_gqa_b1hq32hkv8s16384d128_causal": Workload("bwd_gqa_b1hq32hkv8s16384d128_causal", 1, 32,
                                                     8, 16384, 16384, 128, True, seed=1003,
                                                     backward=True),
+    # head dimension 256 (the same FLOPs as the d = 128 prefill shape: half the heads)
+    "d256_b2h16s8192_causal": Workload("d256_b2h16s8192_causal", 2, 16, 16, 8192, 8192, 256,
+                                       True, seed=1007),
     # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
     "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
                                           True, dtype="f16", seed=1005),

@@ -50,7 +50,8 @@ typedef enum {
     ATTN_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, Hq % Hkv != 0,
                                  scale not finite and > 0, an index that does
                                  not fit in 32 bits */
-    ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128}, unknown dtype, device is
+    ATTN_ERR_UNSUPPORTED = 2, /* d not in {64, 128} (or 256 outside attn_fwd's
+                                 bf16 / fp16 path), unknown dtype, device is
                                  not compute capability 10.3 (B300) */
     ATTN_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned (TMA rule) */
     ATTN_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
@@ -73,7 +74,10 @@ typedef enum {
  *   q, k, v : device inputs in the layouts above, element type `dtype`
  *   o       : device output [B, Sq, Hq, d]: fp16 for ATTN_F16, else bf16
  *   lse     : device output, fp32 [B, Hq, Sq]
- *   B, Hq, Hkv, Sq, Sk, d : sizes; Hq % Hkv == 0; d in {64, 128}
+ *   B, Hq, Hkv, Sq, Sk, d : sizes; Hq % Hkv == 0; d in {64, 128}, or 256
+ *             for ATTN_BF16 / ATTN_F16 (a kernel with one 128-row Q tile per
+ *             unit and 64-key K/V tiles, since two d = 256 O accumulators do
+ *             not fit the tensor memory beside the scores)
  *   causal  : 0 or non-zero (bottom-right causal mask)
  *   scale   : softmax scale applied to Q.K (finite, > 0; usually 1/sqrt(d))
  *   dtype   : attn_dtype_t; ATTN_FP8_E4M3 behaves as attn_fwd_fp8 with all

@@ -73,7 +73,8 @@ def fwd(**kw):
     (dict(scale=float("inf")), ea.ATTN_ERR_INVALID_ARG),
     (dict(B=1, Sq=1 << 20, Hq=32, Hkv=32, d=128), ea.ATTN_ERR_INVALID_ARG),  # 2^32 elements
     (dict(d=96), ea.ATTN_ERR_UNSUPPORTED),
-    (dict(d=256), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=192), ea.ATTN_ERR_UNSUPPORTED),
+    (dict(d=256, dtype=ea.ATTN_FP8_E4M3), ea.ATTN_ERR_UNSUPPORTED),
     (dict(dtype=7), ea.ATTN_ERR_UNSUPPORTED),
     (dict(q=Q + 8), ea.ATTN_ERR_MISALIGNED),
     (dict(v=V + 2), ea.ATTN_ERR_MISALIGNED),
@@ -241,3 +242,17 @@ def test_bwd_rejects_bad_arguments(lib, kw, code):
                      a["dv"], a["B"], a["Hq"], a["Hkv"], a["Sq"], a["Sk"], a["d"], a["causal"],
                      a["scale"], a["dtype"], a["workspace"], a["workspace_bytes"], stream=0)
     assert rc == code
+
+
+def test_d256_is_forward_only(lib):
+    """Head dimension 256 is served by attn_fwd (bf16 / fp16) only."""
+    assert ea.attn_fwd(Q, K, V, O, L, 1, 2, 2, 64, 64, 256, 1, 0.1, ea.ATTN_FP8_E4M3,
+                       stream=0) == ea.ATTN_ERR_UNSUPPORTED
+    assert ea.attn_fwd_fp8(Q, K, V, 0x60000, 0x60100, 0x60200, O, L, 1, 2, 2, 64, 64, 256, 1,
+                           0.1, stream=0) == ea.ATTN_ERR_UNSUPPORTED
+    assert ea.attn_fwd_splitkv(Q, K, V, O, L, 1, 2, 2, 64, 1000, 256, 0, 0.1, ea.ATTN_BF16, 2,
+                               0x60000, 1 << 30, stream=0) == ea.ATTN_ERR_UNSUPPORTED
+    assert ea.attn_bwd(Q, K, V, O, L, 0x70000, 0xA0000, 0xB0000, 0xD0000, 1, 2, 2, 64, 64, 256,
+                       1, 0.1, ea.ATTN_BF16, 0xC0000, 1 << 20, stream=0) == ea.ATTN_ERR_UNSUPPORTED
+    assert ea.attn_fwd(Q, K, V, O, L, 1, 2, 2, 64, 64, 192, 1, 0.1, ea.ATTN_BF16,
+                       stream=0) == ea.ATTN_ERR_UNSUPPORTED
