@@ -14,16 +14,15 @@
 //           ahead into buffer j & 1;  O += P(j) V_j  (M = 128, N = 256,
 //           K = 64, P from TMEM)
 //   issue   S(0) S(1) | <-P(0) PV(0) S(2) | <-P(1) PV(1) S(3) | ...
-// so the softmax of tile j+1 overlaps PV(j) and S(j+2). P has buffers of its
-// own: issued right behind PV(j), S(j+2) would otherwise write the columns
-// PV(j) reads its A operand from, and at N = 256 that overlap corrupted P
-// (the d = 128 kernels, whose P aliases S, keep a full product between the
-// two). The softmax writes P(j) only after S(j) has completed, which implies
-// PV(j-2), the buffer's previous reader, has too. The P barrier is per
-// buffer as well: S(j+1) is already complete when a warp finishes P(j), so a
-// fast warp can arrive for tile j+1 before a slow one has arrived for tile j;
-// with one barrier that early arrival would complete tile j's phase. It
-// cannot run two tiles ahead, because S(j+2) waits for PV(j). Because the next S is
+// so the softmax of tile j+1 overlaps PV(j) and S(j+2). P sits in buffers of
+// its own (TMEM has the room; P packed into the S buffer, as the d = 128
+// kernels do, measured the same): the softmax writes P(j) only after S(j) has
+// completed, which implies PV(j-2), the buffer's previous reader, has too.
+// The P barrier is per buffer: S(j+1) is already complete when a warp
+// finishes P(j), so a fast warp can arrive for tile j+1 before a slow one has
+// arrived for tile j, and with one barrier that early arrival would complete
+// tile j's phase. A warp cannot run two tiles ahead, because S(j+2) waits
+// for PV(j). Because the next S is
 // already in flight, "S(j+1) complete" no longer implies "PV(j) complete":
 // a softmax step that must rescale O first waits for pv_done of PV(j).
 //
