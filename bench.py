@@ -47,6 +47,9 @@ KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
                   "exact_attention_forward_14_b300/csrc/ptx.cuh"]
 KERNEL_SOURCES_BWD = ["exact_attention_forward_14_b300/csrc/attn_bwd_kernel.cuh",
                       "exact_attention_forward_14_b300/csrc/ptx.cuh"]
+KERNEL_SOURCES_D256 = ["exact_attention_forward_14_b300/csrc/attn_fwd_d256.cuh",
+                       "exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
+                       "exact_attention_forward_14_b300/csrc/ptx.cuh"]
 PROFILES = os.path.join(ROOT, "profiles")
 
 
@@ -543,10 +546,12 @@ def run_ours(args, w):
     roofline = {
         "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
         "frac": achieved / peak,
-        "traffic": ncu_traffic(w.name, KERNEL_SOURCES_BWD if bwd is not None else KERNEL_SOURCES),
+        "traffic": ncu_traffic(w.name, KERNEL_SOURCES_BWD if bwd is not None else
+                               KERNEL_SOURCES_D256 if w.d == 256 else KERNEL_SOURCES),
         "kernel": (f"attn_bwd (bwd_prep_kernel + bwd_dkdv_kernel + bwd_dq_kernel)<{w.d},"
                    f"{str(w.dtype == 'f16').lower()}>, executed FLOPs (7 products per pair)"
                    if bwd is not None else
+                   f"attn_fwd_d256_kernel<{str(w.dtype == 'f16').lower()}>" if w.d == 256 else
                    f"attn_fwd_kernel<{w.d},{str(w.dtype == 'e4m3').lower()},"
                    f"{str(w.dtype == 'f16').lower()}>"),
         "peak_source": (f"{peaks_src} bf16 burst" if w.dtype != "e4m3"

@@ -165,3 +165,34 @@ def test_backward_full_size_sampled(oracle_mod, name, nkv):
     assert_grad_close("dq", gather(dq, qrows, w.Hq, w.Sq), rq)
     assert_grad_close("dk", gather(dk, krows, w.Hkv, w.Sk), rk)
     assert_grad_close("dv", gather(dv, krows, w.Hkv, w.Sk), rv)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_long_key_side(oracle_mod, causal):
+    """Sq = 256 against Sk = 131072 (1024 key tiles, GQA 4:1): dQ at sampled
+    rows and dK, dV at sampled keys (the first and last keys included; under
+    the bottom-right causal mask every key is seen by some row)."""
+    torch = require_gpu()
+    B, Hq, Hkv, Sq, Sk, d = 1, 4, 1, 256, 131072, 128
+    q, k, v = inputs.draw_qkv_bf16(B, Hq, Hkv, Sq, Sk, d, seed=31)
+    do = inputs.draw_grad_out(B, Sq, Hq, d, 31)
+    scale = d ** -0.5
+    qd, kd, vd, dod = (t.cuda() for t in (q, k, v, do))
+    o, lse = ea.forward(qd, kd, vd, causal=causal, scale=scale)
+    dq, dk, dv = ea.backward(qd, kd, vd, o, lse, dod, causal=causal, scale=scale)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    qrows = inputs.sample_rows(B, Hq, Sq, 24, seed=5)
+    rng = np.random.default_rng(6)
+    krows = np.array(sorted(set(int(x) for x in rng.choice(Sk, size=30, replace=False)) |
+                            {0, Sk - 1, Sk - Sq, Sk - 1 - Sq}), dtype=np.int64)
+    rq, rk, rv = oracle_mod.attn_bwd_sampled(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
+                                             inputs.bits16(do), causal, scale, qrows, krows)
+    b, rem = np.divmod(qrows, Hq * Sq)
+    h, i = np.divmod(rem, Sq)
+    gq = dq[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
+    gk = dk[0, torch.as_tensor(krows), 0].float().cpu().numpy()
+    gv = dv[0, torch.as_tensor(krows), 0].float().cpu().numpy()
+    assert_grad_close("dq", gq, rq)
+    assert_grad_close("dk", gk, rk)
+    assert_grad_close("dv", gv, rv)
