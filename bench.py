@@ -293,6 +293,36 @@ def job_tflops(flops_per_step: float, steps: int, world: int, total_ms: float) -
     return world * flops_per_step * steps / (total_ms * 1e-3) / 1e12
 
 
+# ------------------------------------------------------ MUFU microbench --
+
+def mufu_ex2_rate(w, num_sms: int, sm_mhz: float):
+    """ex2.approx throughput per SM per clock from the self-test library's
+    microbenchmark (one CTA per SM), and the TFLOP/s ceiling it would set on
+    its own: every score element needs one exp2 and 4 d tensor FLOPs."""
+    import ctypes
+    import statistics as st
+    import torch
+    path = os.path.join(ROOT, "exact_attention_forward_14_b300", "libattn_selftest.so")
+    lib = ctypes.CDLL(path)
+    lib.attn_selftest_ex2_rate.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_void_p,
+                                           ctypes.c_void_p, ctypes.c_void_p]
+    lib.attn_selftest_ex2_rate.restype = ctypes.c_int
+    iters = 2048
+    cyc = torch.zeros(num_sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1024, dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream or None
+    for _ in range(2):  # the first launch warms the clocks and the instruction cache
+        rc = lib.attn_selftest_ex2_rate(iters, num_sms, cyc.data_ptr(), sink.data_ptr(), stream)
+        if rc != 0:
+            return None
+    rates = [1024 * 8 * iters / c for c in cyc.cpu().tolist() if c > 0]
+    rate = st.median(rates)
+    ceiling = rate * num_sms * sm_mhz * 1e6 * 4 * w.d / 1e12
+    return {"ex2_per_clk_per_sm": rate, "implied_ceiling_tflops": ceiling,
+            "note": "one exp2 per score element against 4 d tensor FLOPs; "
+                    "microbenchmark in csrc/mufu_rate.cu"}
+
+
 # ------------------------------------------------------------- GPU path --
 
 def e2e_backward(args, w, host, dev_in, o, lse, bwd, step, stream, dev, dist, world, flops):
@@ -572,6 +602,10 @@ def run_ours(args, w):
     }
     if prologue_line is not None:
         line["prologue"] = prologue_line
+    if not w.backward:
+        props = torch.cuda.get_device_properties(dev)
+        clk = line["clocks"].get("sm_mhz") or 2032.0
+        line["mufu"] = mufu_ex2_rate(w, props.multi_processor_count, float(clk))
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)

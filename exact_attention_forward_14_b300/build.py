@@ -4,7 +4,8 @@
 
 Produces, next to this file:
   libattn_b300.so           the attention library (C ABI in include/attn_b300.h)
-  libattn_selftest.so       single-tile tensor-core layout checks used by the tests
+  libattn_selftest.so       single-tile tensor-core layout checks used by the tests, and
+                            the MUFU exp2 throughput microbenchmark
   libattn_watchdog_test.so  test-only build of the library whose Q barrier is
                             never armed, so every launch ends through the
                             watchdog (bounded wait -> ATTN_ERR_TIMEOUT)
@@ -33,7 +34,7 @@ NVCC_FLAGS = [
 # name -> (sources, extra nvcc flags)
 TARGETS = {
     "libattn_b300.so": (["attn_api.cu"], []),
-    "libattn_selftest.so": (["selftest_umma.cu"], []),
+    "libattn_selftest.so": (["selftest_umma.cu", "mufu_rate.cu"], []),
     "libattn_watchdog_test.so": (["attn_api.cu"], ["-DATTN_TEST_NEVER_ARM_Q"]),
 }
 

@@ -63,3 +63,24 @@ def test_umma_bf16(form):
 @pytest.mark.parametrize("form", [0, 1], ids=["qk", "pv"])
 def test_umma_fp8(form):
     _single_tile(form, 1)
+
+
+@pytest.mark.gpu
+def test_mufu_ex2_rate_is_measured():
+    """The exp2 throughput microbenchmark runs on every SM and reports a
+    plausible per-SM rate (the SFU issues a warp's ex2 over a few cycles per
+    scheduler: between 8 and 128 results per clock per SM)."""
+    torch = require_gpu()
+    lib = ctypes.CDLL(LIB)
+    lib.attn_selftest_ex2_rate.argtypes = [ctypes.c_int, ctypes.c_int] + [ctypes.c_void_p] * 3
+    lib.attn_selftest_ex2_rate.restype = ctypes.c_int
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    sink = torch.zeros(1024, dtype=torch.float32, device="cuda")
+    for _ in range(2):
+        assert lib.attn_selftest_ex2_rate(1024, sms, cyc.data_ptr(), sink.data_ptr(), None) == 0
+    rates = [1024 * 8 * 1024 / c for c in cyc.cpu().tolist()]
+    assert all(c > 0 for c in cyc.cpu().tolist())
+    med = sorted(rates)[len(rates) // 2]
+    print(f"ex2 per clock per SM: median {med:.2f}, min {min(rates):.2f}, max {max(rates):.2f}")
+    assert 8.0 <= med <= 128.0
