@@ -199,12 +199,14 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
         if (st == 0) break;
         if (st == 1 || U.n == 0) continue;
         if (!wait_bounded(BAR_Q_EMPTY, (qit & 1u) ^ 1u, ctl, P)) { ok = false; break; }
+#ifndef ATTN_TEST_NEVER_ARM_Q
         mbar_arrive_expect_tx(BAR_Q_FULL, C::Q_BYTES);
 #pragma unroll
         for (int c = 0; c < C::NCHUNK; ++c)
           tma_load_4d(sbase + C::OFF_Q + c * C::Q_CH, &tm_q, BAR_Q_FULL, c * C::CHUNK_ELEMS, U.hq,
                       U.row0, U.b);
         ++qit;
+#endif  // (watchdog test library: Q never loaded, q_full never completes)
         for (int j = 0; ok && j < U.n; ++j) {
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {
