@@ -256,3 +256,14 @@ def test_d256_is_forward_only(lib):
                        1, 0.1, ea.ATTN_BF16, 0xC0000, 1 << 20, stream=0) == ea.ATTN_ERR_UNSUPPORTED
     assert ea.attn_fwd(Q, K, V, O, L, 1, 2, 2, 64, 64, 192, 1, 0.1, ea.ATTN_BF16,
                        stream=0) == ea.ATTN_ERR_UNSUPPORTED
+
+
+def test_bwd_rejects_padded_row_statistics_past_32_bits(lib):
+    """Sq = 1 pads to a 128-row tile: 20M (b, hq) pairs keep every tensor below
+    2^31 elements (20M x 64) but the padded statistics (20M x 128 rows) past
+    it, so the call is refused on the host."""
+    B, Hq = 2, 10_000_000
+    assert B * 1 * Hq * 64 < 2 ** 31 < B * Hq * 128
+    rc = ea.attn_bwd(Q, K, V, O, L, 0x70000, 0xA0000, 0xB0000, 0xD0000, B, Hq, Hq, 1, 1, 64, 0,
+                     0.1, ea.ATTN_BF16, 0xC0000, 1 << 40, stream=0)
+    assert rc == ea.ATTN_ERR_INVALID_ARG
