@@ -325,36 +325,57 @@ def mufu_ex2_rate(w, num_sms: int, sm_mhz: float):
 
 # ------------------------------------------------------------- GPU path --
 
-def e2e_backward(args, w, host, dev_in, o, lse, bwd, step, stream, dev, dist, world, flops):
-    """The backward step end to end: its inputs (q, k, v, O, LSE, dO) copied
-    from pinned host memory, attn_bwd, and dQ, dK, dV copied back, every step."""
+def e2e_pipelined(args, host_in, bufs, step, dev, dist, world, flops):
+    """The step end to end through the public call: each step's inputs are
+    copied from pinned host memory to the device and its outputs back, as a
+    caller streaming many problems would do it. Three streams and two buffer
+    sets overlap step k's compute with the copies of steps k-1 and k+1, and
+    the two copy directions with each other; every step still moves all of
+    its own bytes. The timed region starts on an idle device (pipeline fill
+    included) and ends when the last result has reached the host."""
     import torch
-    h_o = o.cpu().pin_memory()
-    h_lse = lse.cpu().pin_memory()
-    hin = list(host) + [h_o, h_lse, bwd["h_do"]]
-    din = list(dev_in) + [o, lse, bwd["do"]]
-    hout = [torch.empty(g.shape, dtype=g.dtype).pin_memory() for g in bwd["grads"]]
+    sets = [bufs, {"in": tuple(torch.empty_like(t) for t in bufs["in"]),
+                   "out": tuple(torch.empty_like(t) for t in bufs["out"])}]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in bufs["out"]]
+                for _ in range(2)]
+    s_in, s_cmp, s_out = (torch.cuda.Stream(dev) for _ in range(3))
     e_steps = max(3, min(args.steps, 20))
-    for it in range(e_steps + 2):
-        if it == 2:
+    n = e_steps + 2
+    ev_in = [torch.cuda.Event() for _ in range(n)]
+    ev_cmp = [torch.cuda.Event() for _ in range(n)]
+    ev_out = [torch.cuda.Event() for _ in range(n)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for k in range(n):
+        b = k % 2
+        if k == 2:  # two untimed steps, then start from an idle device
+            torch.cuda.synchronize(dev)
             if dist is not None:
                 dist.barrier()
-            torch.cuda.synchronize(dev)
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-        for dst, src in zip(din, hin):
-            dst.copy_(src, non_blocking=True)
-        step()
-        for dst, src in zip(hout, bwd["grads"]):
-            dst.copy_(src, non_blocking=True)
-    e1.record(stream)
+            e0.record(s_in)
+        if k >= 2:
+            s_in.wait_event(ev_cmp[k - 2])  # step k-2 has finished reading set b
+        with torch.cuda.stream(s_in):
+            for dst, src in zip(sets[b]["in"], host_in):
+                dst.copy_(src, non_blocking=True)
+        ev_in[k].record(s_in)
+        s_cmp.wait_event(ev_in[k])
+        if k >= 2:
+            s_cmp.wait_event(ev_out[k - 2])  # set b's outputs of step k-2 are on the host
+        step(sets[b], s_cmp.cuda_stream)
+        ev_cmp[k].record(s_cmp)
+        s_out.wait_event(ev_cmp[k])
+        with torch.cuda.stream(s_out):
+            for dst, src in zip(host_out[b], sets[b]["out"]):
+                dst.copy_(src, non_blocking=True)
+        ev_out[k].record(s_out)
+    e1.record(s_out)
     torch.cuda.synchronize(dev)
     e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     return {"value": job_tflops(flops, e_steps, world, e_ms), "unit": "TFLOP/s",
-            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hin),
-            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in hout),
-            "ms_per_step": e_ms / e_steps}
+            "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+            "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in bufs["out"]),
+            "ms_per_step": e_ms / e_steps,
+            "pipelined": "3 streams, 2 buffer sets: copies overlap neighbouring steps' compute"}
 
 
 def run_ours(args, w):
@@ -427,44 +448,50 @@ def run_ours(args, w):
         wk = inputs.draw_norm_weights(w.Hkv * w.d, w.seed + 51, w.dtype).to(dev)
         norm = (wq, wk, torch.empty_like(dev_in[0]), torch.empty_like(dev_in[1]))
 
-    def prologue():
-        q, k, _ = dev_in[:3]
+    code16 = ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16
+    # one step's device buffers: its inputs (copied in by the e2e leg) and its outputs
+    if bwd is not None:
+        default_bufs = {"in": tuple(dev_in) + (o, lse, bwd["do"]), "out": bwd["grads"]}
+    else:
+        default_bufs = {"in": tuple(dev_in), "out": (o, lse)}
+
+    def prologue(bufs=default_bufs, st=None):
+        q, k = bufs["in"][0], bufs["in"][1]
         wq, wk, qn, kn = norm
         rc = ea.attn_qk_rmsnorm(q, k, wq, wk, qn, kn, w.B, w.Sq, w.Sk, w.Hq, w.Hkv, w.d, 1e-6,
-                                ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
+                                code16, st if st is not None else stream)
         if rc != ea.ATTN_OK:
             raise ea.AttnError(rc, "attn_qk_rmsnorm")
         return qn, kn
 
-    def step():
+    def step(bufs=default_bufs, st=None):
+        st = st if st is not None else stream
         if bwd is not None:
-            q, k, v = dev_in
-            dq, dk, dv = bwd["grads"]
-            rc = ea.attn_bwd(q, k, v, o, lse, bwd["do"], dq, dk, dv, w.B, w.Hq, w.Hkv, w.Sq,
+            q, k, v, o_, lse_, d_o = bufs["in"]
+            dq, dk, dv = bufs["out"]
+            rc = ea.attn_bwd(q, k, v, o_, lse_, d_o, dq, dk, dv, w.B, w.Hq, w.Hkv, w.Sq,
                              w.Sk, w.d, w.causal, w.scale, bwd["code"], bwd["ws"],
-                             bwd["ws"].numel() * 4, stream)
+                             bwd["ws"].numel() * 4, st)
             if rc != ea.ATTN_OK:
                 raise ea.AttnError(rc, "attn_bwd")
             return
+        o_, lse_ = bufs["out"]
         if norm is not None:
-            qn, kn = prologue()
-            rc = ea.attn_fwd(qn, kn, dev_in[2], o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
-                             w.causal, w.scale,
-                             ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
+            qn, kn = prologue(bufs, st)
+            rc = ea.attn_fwd(qn, kn, bufs["in"][2], o_, lse_, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
+                             w.causal, w.scale, code16, st)
         elif ws is not None:
-            q, k, v = dev_in
-            rc = ea.attn_fwd_splitkv(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
-                                     w.causal, w.scale,
-                                     ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, nsplit,
-                                     ws, ws.numel() * 4, stream)
+            q, k, v = bufs["in"]
+            rc = ea.attn_fwd_splitkv(q, k, v, o_, lse_, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d,
+                                     w.causal, w.scale, code16, nsplit, ws, ws.numel() * 4, st)
         elif w.dtype == "e4m3":
-            q8, k8, v8, qs, ks, vs = dev_in
-            rc = ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk,
-                                 w.d, w.causal, w.scale, stream)
+            q8, k8, v8, qs, ks, vs = bufs["in"]
+            rc = ea.attn_fwd_fp8(q8, k8, v8, qs, ks, vs, o_, lse_, w.B, w.Hq, w.Hkv, w.Sq, w.Sk,
+                                 w.d, w.causal, w.scale, st)
         else:
-            q, k, v = dev_in
-            rc = ea.attn_fwd(q, k, v, o, lse, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal,
-                             w.scale, ea.ATTN_F16 if w.dtype == "f16" else ea.ATTN_BF16, stream)
+            q, k, v = bufs["in"]
+            rc = ea.attn_fwd(q, k, v, o_, lse_, w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.causal,
+                             w.scale, code16, st)
         if rc != ea.ATTN_OK:
             raise ea.AttnError(rc, "attn_fwd")
 
@@ -503,40 +530,14 @@ def run_ours(args, w):
     flops = w.flops()
     value = job_tflops(flops, args.steps, world, total_ms)
 
-    # end to end through the public API: pinned host inputs -> device -> kernel
-    # -> O and LSE back to pinned host memory, every step
+    # end to end through the public API: every step copies its inputs from
+    # pinned host memory and reads its results back (see e2e_pipelined)
     e2e = None
-    if host is not None and bwd is not None:
-        e2e = e2e_backward(args, w, host, dev_in, o, lse, bwd, step, stream, dev, dist, world,
-                           flops)
-    elif host is not None:
-        ho = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        hl = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-        e_steps = max(3, min(args.steps, 20))
-        dq, dk, dv = dev_in
-        for it in range(e_steps + 2):
-            if it == 2:
-                if dist is not None:
-                    dist.barrier()
-                torch.cuda.synchronize(dev)
-                e0 = torch.cuda.Event(enable_timing=True)
-                e1 = torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-            dq.copy_(host[0], non_blocking=True)
-            dk.copy_(host[1], non_blocking=True)
-            dv.copy_(host[2], non_blocking=True)
-            step()
-            ho.copy_(o, non_blocking=True)
-            hl.copy_(lse, non_blocking=True)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        e_ms = e0.elapsed_time(e1)
-        e_ms = max_over_ranks(e_ms, dist, dev)
-        h2d = sum(t.numel() * t.element_size() for t in host)
-        d2h = o.numel() * o.element_size() + lse.numel() * lse.element_size()
-        e2e = {"value": job_tflops(flops, e_steps, world, e_ms), "unit": "TFLOP/s",
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms / e_steps}
+    if host is not None:
+        host_in = list(host)
+        if bwd is not None:
+            host_in += [o.cpu().pin_memory(), lse.cpu().pin_memory(), bwd["h_do"]]
+        e2e = e2e_pipelined(args, host_in, default_bufs, step, dev, dist, world, flops)
 
     prologue_line = None
     if norm is not None:
