@@ -99,7 +99,7 @@ int attn_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
  *   k_scale,
  *   v_scale    : fp32 [B, Hkv, ceil(Sk / 64)]
  * The value of an element is code * scale of its (b, h, row / 64) block.
- * Scales must be finite and > 0. Other arguments as attn_fwd.
+ * Scales must be finite and > 0. Other arguments as attn_fwd, with d in {64, 128}.
  */
 int attn_fwd_fp8(const void* q, const void* k, const void* v,
                  const float* q_scale, const float* k_scale, const float* v_scale,
@@ -128,7 +128,7 @@ int attn_splitkv_plan(int B, int Hq, int Sq, int Sk, int d, int causal, int num_
  * processed by separate work items, merged by a second kernel (the online-
  * softmax rescaling of the FlashAttention-3 deep dive, sections 2-3, applied
  * across key ranges: LSE = ln sum_s exp(LSE_s), O = sum_s exp(LSE_s - LSE) O_s).
- * Arguments as attn_fwd (dtype ATTN_BF16 or ATTN_F16), plus:
+ * Arguments as attn_fwd (dtype ATTN_BF16 or ATTN_F16, d in {64, 128}), plus:
  *   num_splits      : requested ranges, 1..256 (ranges of ceil(Sk/128/n) K/V
  *                     tiles; fewer if some would be empty)
  *   workspace       : device buffer owned by the caller, 16-byte aligned, at
@@ -237,7 +237,7 @@ int attn_bwd_workspace_size(int B, int Hq, int Sq, size_t* workspace_bytes);
  *   workspace  : device buffer owned by the caller, 16-byte aligned, at least
  *                attn_bwd_workspace_size bytes; contents on entry ignored, on
  *                return undefined
- * Other arguments as attn_fwd. P and dS are rounded to dtype before they
+ * Other arguments as attn_fwd, with d in {64, 128}. P and dS are rounded to dtype before they
  * enter the tensor cores (fp32 accumulation); the gradients are rounded to
  * nearest in dtype. Three kernels are enqueued on `stream` (row statistics,
  * dK/dV, dQ); every output element is written exactly once, so results are
