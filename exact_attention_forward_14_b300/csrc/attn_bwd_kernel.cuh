@@ -3,8 +3,9 @@
 // The pages describe the forward pass only. The backward pass here is the
 // chain rule through the same definition, O = softmax(scale Q K^T + mask) V,
 // evaluated tile by tile like the forward of the FlashAttention-3 deep dive
-// (techknowgenie.com/posts/109164421204410442, "IO-aware tiling": the score
-// and probability matrices never reach HBM):
+// (techknowgenie.com/posts/109164421204410442, introduction: I/O-aware tiling
+// with an online softmax, so the score and probability matrices never reach
+// HBM):
 //   P  = exp(scale Q K^T - LSE)       (recomputed from the forward's LSE)
 //   dV = P^T dO,  dP = dO V^T,  D = rowsum(dO * O),  dS = P * (dP - D)
 //   dQ = scale dS K,  dK = scale dS^T Q
