@@ -284,6 +284,12 @@ def backward(q, k, v, o, lse, d_o, causal: bool = False, scale: float | None = N
     import torch
     B, Sq, Hq, d = q.shape
     _, Sk, Hkv, _ = k.shape
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError(f"backward takes bf16 or fp16 tensors, not {q.dtype}")
+    if any(t.dtype != q.dtype for t in (k, v, o, d_o)):
+        raise TypeError("q, k, v, o and d_o must share one dtype")
+    if lse.dtype != torch.float32:
+        raise TypeError("lse must be float32")
     code = ATTN_F16 if q.dtype == torch.float16 else ATTN_BF16
     if scale is None:
         scale = 1.0 / math.sqrt(d)

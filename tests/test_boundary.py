@@ -267,3 +267,17 @@ def test_bwd_rejects_padded_row_statistics_past_32_bits(lib):
     rc = ea.attn_bwd(Q, K, V, O, L, 0x70000, 0xA0000, 0xB0000, 0xD0000, B, Hq, Hq, 1, 1, 64, 0,
                      0.1, ea.ATTN_BF16, 0xC0000, 1 << 40, stream=0)
     assert rc == ea.ATTN_ERR_INVALID_ARG
+
+
+def test_backward_wrapper_checks_dtypes():
+    """The tensor convenience refuses mixed or unsupported dtypes on the host."""
+    import torch
+    q = torch.zeros(1, 4, 1, 64, dtype=torch.bfloat16)
+    f = torch.zeros(1, 4, 1, 64, dtype=torch.float16)
+    lse = torch.zeros(1, 1, 4, dtype=torch.float32)
+    with pytest.raises(TypeError):
+        ea.backward(q, q, q, q, lse, f)
+    with pytest.raises(TypeError):
+        ea.backward(q, q, q, q, lse.double(), q)
+    with pytest.raises(TypeError):
+        ea.backward(q.float(), q.float(), q.float(), q.float(), lse, q.float())
