@@ -242,7 +242,9 @@ int attn_bwd_workspace_size(int B, int Hq, int Sq, size_t* workspace_bytes);
  * nearest in dtype. Three kernels are enqueued on `stream` (row statistics,
  * dK/dV, dQ); every output element is written exactly once, so results are
  * deterministic. Calls that share a workspace must not overlap. Errors as
- * attn_fwd; ATTN_ERR_INVALID_ARG for a missing or too small workspace.
+ * attn_fwd; ATTN_ERR_INVALID_ARG for a missing or too small workspace or for
+ * B * Hq * Sq_pad >= 2^31, ATTN_ERR_MISALIGNED for a workspace or gradient
+ * pointer not 16-byte aligned, ATTN_ERR_UNSUPPORTED for d = 256 or E4M3.
  */
 int attn_bwd(const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* d_o, void* dq, void* dk, void* dv, int B, int Hq, int Hkv, int Sq,
