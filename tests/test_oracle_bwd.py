@@ -148,3 +148,25 @@ def test_sampled_gradients_equal_the_whole(oracle_mod, causal):
     np.testing.assert_allclose(sq, dq_flat[qrows], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(sk, dk_flat[krows], rtol=1e-12, atol=1e-14)
     np.testing.assert_allclose(sv, dv_flat[krows], rtol=1e-12, atol=1e-14)
+
+
+def test_f16_gradients_equal_bf16_gradients_on_shared_values(oracle_mod):
+    """Multiples of 1/256 up to +-200/256 are exact in both bf16 and fp16, so
+    the backward pass's two 16-bit input paths (whole and sampled) must give
+    identical gradients on them: the input type only changes the decoding."""
+    B, Hq, Hkv, Sq, Sk, d = 1, 4, 2, 19, 23, 8
+    (qb, qv), (kb, kv), (vb, vv), (dob, dov) = make_case(21, B, Hq, Hkv, Sq, Sk, d)
+    as_f16 = [torch.tensor(x, dtype=torch.float16).view(torch.int16).numpy().view(np.uint16)
+              for x in (qv, kv, vv, dov)]
+    qrows = np.array([0, 5, B * Hq * Sq - 1])
+    krows = np.array([1, 7, B * Hkv * Sk - 1])
+    for causal in (False, True):
+        got = oracle_mod.attn_bwd(*as_f16, causal, 0.4, dtype="f16")
+        want = oracle_mod.attn_bwd(qb, kb, vb, dob, causal, 0.4, dtype="bf16")
+        for g, w in zip(got, want):
+            np.testing.assert_array_equal(g, w)
+        got = oracle_mod.attn_bwd_sampled(*as_f16, causal, 0.4, qrows, krows, dtype="f16")
+        want = oracle_mod.attn_bwd_sampled(qb, kb, vb, dob, causal, 0.4, qrows, krows,
+                                           dtype="bf16")
+        for g, w in zip(got, want):
+            np.testing.assert_array_equal(g, w)
