@@ -281,3 +281,16 @@ def test_backward_wrapper_checks_dtypes():
         ea.backward(q, q, q, q, lse.double(), q)
     with pytest.raises(TypeError):
         ea.backward(q.float(), q.float(), q.float(), q.float(), lse, q.float())
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    """Without the built library every entry point raises: there is no
+    non-CUDA fallback for a caller to land on silently."""
+    monkeypatch.setattr(ea, "_lib", None)
+    monkeypatch.setattr(ea, "library_path", lambda: str(tmp_path / "libattn_b300.so"))
+    with pytest.raises(ImportError, match="no non-CUDA fallback"):
+        ea.load()
+    with pytest.raises(ImportError):
+        ea.attn_fwd(Q, K, V, O, L, 1, 1, 1, 64, 64, 64, 0, 0.1, stream=0)
+    with pytest.raises(ImportError):
+        ea.attn_bwd_workspace_size(1, 1, 1)
