@@ -415,6 +415,49 @@ def e2e_pipelined(args, host_in, bufs, step, dev, dist, world, flops):
             "pipelined": "3 streams, 2 buffer sets: copies overlap neighbouring steps' compute"}
 
 
+def gemm_peaks(n: int = 8192, reps: int = 40):
+    """Library GEMM rates on this GPU at n x n x n, as context for the FP8
+    roofline: cuBLASLt E4M3 x E4M3 -> bf16 (torch._scaled_mm, unit tensor
+    scales, with and without fast accumulation) beside a cuBLAS bf16 matmul.
+    Inputs are N(0,1) draws; each figure is the mean of `reps` back-to-back
+    calls after 5 warm-ups, timed with CUDA events. Prints one JSON line."""
+    import torch
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = torch.Generator(device=dev).manual_seed(7)
+    a16 = torch.randn(n, n, device=dev, generator=g).to(torch.bfloat16)
+    b16 = torch.randn(n, n, device=dev, generator=g).to(torch.bfloat16)
+    a8 = a16.to(torch.float8_e4m3fn)
+    b8 = b16.to(torch.float8_e4m3fn).t()  # column-major second operand
+    one = torch.ones((), device=dev, dtype=torch.float32)
+    calls = {
+        "bf16": lambda: torch.matmul(a16, b16),
+        "fp8": lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                        out_dtype=torch.bfloat16),
+        "fp8_fast_accum": lambda: torch._scaled_mm(a8, b8, scale_a=one, scale_b=one,
+                                                   out_dtype=torch.bfloat16,
+                                                   use_fast_accum=True),
+    }
+    out = {"n": n, "reps": reps}
+    clocks = ClockSampler(0).start()
+    with clocks:
+        for name, f in calls.items():
+            for _ in range(5):
+                f()
+            torch.cuda.synchronize(dev)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                f()
+            e1.record()
+            torch.cuda.synchronize(dev)
+            out[f"{name}_tflops"] = 2.0 * n ** 3 / (e0.elapsed_time(e1) / reps * 1e-3) / 1e12
+    out["fp8_over_bf16"] = max(out["fp8_tflops"], out["fp8_fast_accum_tflops"]) / out["bf16_tflops"]
+    out["clocks"] = clocks.summary()
+    print(json.dumps(out), flush=True)
+    return 0
+
+
 def run_ours(args, w):
     import torch
     import exact_attention_forward_14_b300 as ea
@@ -699,7 +742,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true",
                     help="skip the CPU oracle timing (e.g. under a profiler)")
+    ap.add_argument("--gemm-peaks", action="store_true",
+                    help="only time library bf16 and FP8 GEMMs (8192^3) and exit")
     args = ap.parse_args(argv)
+    if args.gemm_peaks:
+        return gemm_peaks()
     from exact_attention_forward_14_b300 import inputs
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
