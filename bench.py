@@ -226,9 +226,23 @@ def _oracle_sample(w, bits, target_s: float, seed: int, n_fixed: int | None = No
         n = int(min(total, max(2 * n, n * target_s / max(dt, 1e-3) * 1.05)))
 
 
+def cpu_model() -> str:
+    """The host CPU's model name (Linux), or the platform's processor string."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or "unknown"
+
+
 def cpu_baseline(w, target_s: float = 12.0):
     flops, dt, n, threads = _oracle_sample(w, _oracle_inputs(w), target_s, seed=1)
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(),
             "sample": f"{n} random query rows of all (b, h) of the workload "
                       f"({flops / 1e9:.1f} GFLOP by the metric's count) in {dt:.1f} s, "
                       + ("fp64 oracle dQ rows (O, LSE recomputed per row), OpenMP"
@@ -257,6 +271,7 @@ def run_reference(args, w):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "cpu": cpu_model(),
                          "sample": f"each step: ~{flops_t[0][2]} random query rows of the "
                                    "workload through the fp64 oracle"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
