@@ -649,8 +649,8 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
         }
         // per-column-half exponent scales. FP8: the first and second 64 keys
         // of the tile are two scale blocks of K and of V; e_* = log2 of the
-        // factor p is multiplied by before rounding to E4M3, inv_* = 1 / that
-        // factor (largest V scale / V block scale).
+        // factor p is multiplied by before it is rounded to fp16 (V block
+        // scale / largest V scale of the head, <= 1), inv_* = 1 / that factor.
         float c_lo = cq, c_hi = cq;
         float e_lo = 0.f, e_hi = 0.f;
         float inv_lo = 1.f, inv_hi = 1.f;
