@@ -221,10 +221,32 @@ static double load_elem(const oracle_inputs* in, const void* base, const float* 
     return oracle_e4m3_decode(((const uint8_t*)base)[idx]) * sc;
 }
 
+/* The d values of row [b, s, h, :] of an operand, decoded exactly to fp64
+ * into out[d]: the same values load_elem gives, element by element. E4M3
+ * codes are decoded through `e4m3` (oracle_e4m3_decode of every code) and
+ * multiplied by the row's block scale. */
+static void load_row(const oracle_inputs* in, const void* base, const float* scale,
+                     const double* e4m3, int S, int H, int b, int s, int h, double* out) {
+    const int d = in->d;
+    size_t idx = (((size_t)b * S + s) * H + h) * (size_t)d;
+    if (in->dtype == ORACLE_DTYPE_BF16) {
+        const uint16_t* p = (const uint16_t*)base + idx;
+        for (int c = 0; c < d; ++c) out[c] = bf16_bits_to_double(p[c]);
+    } else if (in->dtype == ORACLE_DTYPE_F16) {
+        const uint16_t* p = (const uint16_t*)base + idx;
+        for (int c = 0; c < d; ++c) out[c] = oracle_f16_decode(p[c]);
+    } else {
+        int nblk = (S + ORACLE_FP8_BLOCK_ROWS - 1) / ORACLE_FP8_BLOCK_ROWS;
+        double sc = (double)scale[((size_t)b * H + h) * nblk + s / ORACLE_FP8_BLOCK_ROWS];
+        const uint8_t* p = (const uint8_t*)base + idx;
+        for (int c = 0; c < d; ++c) out[c] = e4m3[p[c]] * sc;
+    }
+}
+
 /* One query row (b, hq, i): writes d outputs to o_row and returns LSE.
- * work: scratch of Sk + 2*d doubles. */
-static double attn_row(const oracle_inputs* in, int causal, double scale, int b, int hq,
-                       int i, double* o_row, double* work) {
+ * work: scratch of Sk + 3*d doubles; e4m3: decode table (E4M3 inputs). */
+static double attn_row(const oracle_inputs* in, const double* e4m3, int causal, double scale,
+                       int b, int hq, int i, double* o_row, double* work) {
     const int d = in->d;
     const int group = in->Hq / in->Hkv;
     const int hkv = hq / group;
@@ -237,18 +259,18 @@ static double attn_row(const oracle_inputs* in, int causal, double scale, int b,
         for (int c = 0; c < d; ++c) o_row[c] = 0.0;
         return -INFINITY;
     }
-    double* s = work;          /* Sk scores */
+    double* s = work;             /* Sk scores */
     double* qrow = work + in->Sk; /* d */
-    double* acc = qrow + d;     /* d */
-    for (int c = 0; c < d; ++c)
-        qrow[c] = load_elem(in, in->q, in->q_scale, in->Sq, in->Hq, b, i, hq, c);
+    double* acc = qrow + d;       /* d */
+    double* kv = acc + d;         /* d: one decoded key or value row */
+    load_row(in, in->q, in->q_scale, e4m3, in->Sq, in->Hq, b, i, hq, qrow);
 
     /* pass 1: scores and their maximum */
     double m = -INFINITY;
     for (long j = 0; j <= jmax; ++j) {
+        load_row(in, in->k, in->k_scale, e4m3, in->Sk, in->Hkv, b, (int)j, hkv, kv);
         double dot = 0.0;
-        for (int c = 0; c < d; ++c)
-            dot += qrow[c] * load_elem(in, in->k, in->k_scale, in->Sk, in->Hkv, b, (int)j, hkv, c);
+        for (int c = 0; c < d; ++c) dot += qrow[c] * kv[c];
         s[j] = scale * dot;
         if (s[j] > m) m = s[j];
     }
@@ -258,8 +280,8 @@ static double attn_row(const oracle_inputs* in, int causal, double scale, int b,
     for (long j = 0; j <= jmax; ++j) {
         double w = exp(s[j] - m);
         l += w;
-        for (int c = 0; c < d; ++c)
-            acc[c] += w * load_elem(in, in->v, in->v_scale, in->Sk, in->Hkv, b, (int)j, hkv, c);
+        load_row(in, in->v, in->v_scale, e4m3, in->Sk, in->Hkv, b, (int)j, hkv, kv);
+        for (int c = 0; c < d; ++c) acc[c] += w * kv[c];
     }
     for (int c = 0; c < d; ++c) o_row[c] = acc[c] / l;
     return m + log(l);
@@ -298,11 +320,11 @@ int oracle_attn_bwd(const void* q, const void* k, const void* v, const void* d_o
     for (int b = 0; b < B; ++b)
         for (int hk = 0; hk < Hkv; ++hk) {
             double* o_row = (double*)malloc(sizeof(double) * 2 * (size_t)d);
-            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 3 * (size_t)d));
             double* dorow = o_row + d;
             for (int hq = hk * group; hq < (hk + 1) * group; ++hq)
                 for (int i = 0; i < Sq; ++i) {
-                    double lse = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+                    double lse = attn_row(&in, NULL, causal, scale, b, hq, i, o_row, work);
                     double* dqrow = dq + (((size_t)b * Sq + i) * Hq + hq) * (size_t)d;
                     for (int c = 0; c < d; ++c) {
                         dqrow[c] = 0.0;
@@ -366,10 +388,10 @@ int oracle_attn_bwd_sampled(const void* q, const void* k, const void* v, const v
         const int bh = (int)(qrows[r] / Sq);
         const int b = bh / Hq, hq = bh % Hq, hk = hq / group;
         double* o_row = (double*)malloc(sizeof(double) * 2 * (size_t)d);
-        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 3 * (size_t)d));
         double* dorow = o_row + d;
         double* out = dq + (size_t)r * d;
-        const double lse = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+        const double lse = attn_row(&in, NULL, causal, scale, b, hq, i, o_row, work);
         double D = 0.0;
         for (int c = 0; c < d; ++c) {
             out[c] = 0.0;
@@ -410,8 +432,8 @@ int oracle_attn_bwd_sampled(const void* q, const void* k, const void* v, const v
             const int g = (int)(gi / Sq), i = (int)(gi % Sq);
             const int hq = hk * group + g;
             double* o_row = (double*)malloc(sizeof(double) * (size_t)d);
-            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
-            lse_all[gi] = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+            double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 3 * (size_t)d));
+            lse_all[gi] = attn_row(&in, NULL, causal, scale, b, hq, i, o_row, work);
             double D = 0.0;
             for (int c = 0; c < d; ++c) D += load_elem(&gin, d_o, NULL, Sq, Hq, b, i, hq, c) * o_row[c];
             D_all[gi] = D;
@@ -474,9 +496,11 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v,
     if (dtype == ORACLE_DTYPE_E4M3 && (!q_scale || !k_scale || !v_scale)) return 1;
     oracle_inputs in = {q, k, v, q_scale, k_scale, v_scale, dtype, B, Hq, Hkv, Sq, Sk, d};
     int64_t total = rows ? nrows : (int64_t)B * Hq * Sq;
+    double e4m3[256];
+    for (int c = 0; c < 256; ++c) e4m3[c] = oracle_e4m3_decode((uint8_t)c);
 #pragma omp parallel
     {
-        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 2 * (size_t)d));
+        double* work = (double*)malloc(sizeof(double) * ((size_t)Sk + 3 * (size_t)d));
 #pragma omp for schedule(dynamic, 4)
         for (int64_t r = 0; r < total; ++r) {
             int64_t flat = rows ? rows[r] : r;
@@ -486,7 +510,7 @@ int oracle_attn_fwd(const void* q, const void* k, const void* v,
             int b = (int)(bh / Hq);
             double* o_row = rows ? o + (size_t)r * d
                                  : o + (((size_t)b * Sq + i) * Hq + hq) * (size_t)d;
-            double val = attn_row(&in, causal, scale, b, hq, i, o_row, work);
+            double val = attn_row(&in, e4m3, causal, scale, b, hq, i, o_row, work);
             lse[rows ? r : flat] = val;
         }
         free(work);
