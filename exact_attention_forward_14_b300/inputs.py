@@ -160,3 +160,18 @@ def sample_rows(B, H, Sq, n, seed):
     pick = set(int(x) for x in g.choice(total, size=min(n, total), replace=False))
     pick.update({0, Sq - 1, total - Sq, total - 1})
     return np.array(sorted(pick), dtype=np.int64)
+
+
+def stratified_rows(B, H, Sq, tile, seed):
+    """Flat row indices (b*H + h)*Sq + i covering every (b, h, tile of `tile`
+    consecutive query rows): the tile's first and last row and one more drawn
+    at random inside it, so every work item of the kernel is checked."""
+    g = np.random.default_rng(seed)
+    ntile = -(-Sq // tile)
+    first = np.arange(ntile, dtype=np.int64) * tile
+    last = np.minimum(first + tile, Sq) - 1
+    pick = []
+    for bh in range(B * H):
+        mid = first + (g.random(ntile) * (last - first + 1)).astype(np.int64)
+        pick.append(bh * Sq + np.unique(np.concatenate([first, last, mid])))
+    return np.unique(np.concatenate(pick))

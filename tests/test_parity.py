@@ -1,13 +1,17 @@
 """GPU parity: the CUDA attention path against the fp64 CPU oracle, on the
-same seeded inputs, through the C ABI. Small shapes are compared element by
-element in full; the full-size workloads (run in the launch configuration the
-benchmark times) on sampled rows."""
+same seeded inputs, through the C ABI. Small shapes, the B4 H16 S2048 causal
+workload and a medium shape that takes the kernel's default pair-order
+schedule are compared element by element in full; the long-context workloads
+(run in the launch configuration the benchmark times) on three rows of every
+(batch, head, 128-row query tile): its first, its last and one at random, so
+every work item the kernel runs is checked. Every case records its strict
+error figures for the end-of-run report."""
 import numpy as np
 import pytest
 
 import exact_attention_forward_14_b300 as ea
 from exact_attention_forward_14_b300 import inputs
-from tests.helpers import assert_lse_close, assert_o_close, bf16_atol, require_gpu
+from tests.helpers import assert_lse_close, assert_o_close, bf16_atol, record, require_gpu
 
 # (B, Hq, Hkv, Sq, Sk, d, causal): several tiles, ragged tails, GQA, Sq != Sk,
 # fully masked rows (causal with Sq > Sk), single row / single key.
@@ -44,8 +48,9 @@ def test_bf16_small_full_compare(oracle_mod, shape):
     o, lse = run_bf16(torch, q, k, v, causal, scale)
     o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
                                          inputs.bf16_bits(v), causal, scale)
-    assert_o_close(o, o_ref)
-    assert_lse_close(lse, lse_ref)
+    st = assert_o_close(o, o_ref)
+    record("small b{}hq{}hkv{}sq{}sk{}d{}{}".format(*shape[:6], "c" if causal else ""), "bf16",
+           st, assert_lse_close(lse, lse_ref), B * Hq * Sq)
 
 
 @pytest.mark.gpu
@@ -84,21 +89,26 @@ def test_repeated_calls_are_deterministic():
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
-def _full_size_rows(oracle_mod, w, n_rows):
-    torch = require_gpu()
-    q, k, v = inputs.draw_qkv_bf16(w.B, w.Hq, w.Hkv, w.Sq, w.Sk, w.d, w.seed)
-    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
-    assert ea.attn_device_status() == ea.ATTN_OK
-    rows = inputs.sample_rows(w.B, w.Hq, w.Sq, n_rows, seed=w.seed)
-    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
-                                         inputs.bf16_bits(v), w.causal, w.scale, rows=rows)
+def _compare_rows(oracle_mod, torch, w, q, k, v, o, lse, rows, case, kind="bf16"):
+    """O and LSE of the listed flat rows (b*Hq + hq)*Sq + i against the oracle."""
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
+                                         w.causal, w.scale, dtype="f16" if kind == "f16" else "bf16",
+                                         rows=rows)
     b, rem = np.divmod(rows, w.Hq * w.Sq)
     h, i = np.divmod(rem, w.Sq)
     o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
     l_g = lse.cpu().numpy()[b, h, i]
-    assert_o_close(o_g, o_ref)
-    assert_lse_close(l_g, lse_ref)
-    assert torch.isfinite(lse).all() and torch.isfinite(o.float()).all()
+    st = assert_o_close(o_g, o_ref, kind=kind)
+    record(case, kind, st, assert_lse_close(l_g, lse_ref), len(rows))
+
+
+def _run_workload(w):
+    torch = require_gpu()
+    q, k, v = inputs.draw_workload_16(w)
+    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
+    assert ea.attn_device_status() == ea.ATTN_OK
+    assert torch.isfinite(lse[lse != float("-inf")]).all() and torch.isfinite(o.float()).all()
+    return torch, q, k, v, o, lse
 
 
 @pytest.mark.gpu
@@ -109,19 +119,59 @@ def test_tiny_workload_full(oracle_mod):
     o, lse = run_bf16(torch, q, k, v, w.causal, w.scale)
     o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
                                          inputs.bf16_bits(v), w.causal, w.scale)
-    assert_o_close(o, o_ref)
-    assert_lse_close(lse, lse_ref)
+    st = assert_o_close(o, o_ref)
+    record(w.name + " (full)", "bf16", st, assert_lse_close(lse, lse_ref), w.B * w.Hq * w.Sq)
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("name,n_rows", [
-    ("b4h16s2048d128_causal", 3000),
-    ("b2h32s8192d128_causal", 1500),
-    ("b2h32s8192d128", 1000),
-    ("gqa_b1hq32hkv8s16384d128_causal", 800),
-])
-def test_full_size_workloads_sampled_rows(oracle_mod, name, n_rows):
-    _full_size_rows(oracle_mod, inputs.WORKLOADS[name], n_rows)
+def test_b4h16s2048_causal_full_compare(oracle_mod):
+    """Every element of the B4 H16 S2048 causal workload (single-unit snake
+    order: 512 units on the SMs)."""
+    w = inputs.WORKLOADS["b4h16s2048d128_causal"]
+    torch, q, k, v, o, lse = _run_workload(w)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
+                                         inputs.bf16_bits(v), w.causal, w.scale)
+    st = assert_o_close(o.float().cpu().numpy(), o_ref)
+    record(w.name + " (full)", "bf16", st, assert_lse_close(lse.cpu().numpy(), lse_ref),
+           w.B * w.Hq * w.Sq)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("name", ["b2h32s8192d128_causal", "b2h32s8192d128",
+                                  "gqa_b1hq32hkv8s16384d128_causal"])
+def test_full_size_workloads_every_tile(oracle_mod, name):
+    """The long-context workloads in the benchmark's launch configuration
+    (pair-order schedule): the first, the last and one random row of every
+    (b, hq, 128-row Q tile)."""
+    w = inputs.WORKLOADS[name]
+    torch, q, k, v, o, lse = _run_workload(w)
+    rows = inputs.stratified_rows(w.B, w.Hq, w.Sq, 128, seed=w.seed)
+    _compare_rows(oracle_mod, torch, w, q, k, v, o, lse, rows, w.name + " (every Q tile)")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("causal", [True, False])
+def test_pair_order_schedule_medium_shape_full(oracle_mod, causal):
+    """A shape with exactly 4 work items per SM, so the host picks the
+    default pair order (heavy level + its mirror per item) rather than the
+    single-unit order small problems get; S = 640 gives an odd number of
+    256-row levels (3), so one item per head runs the middle level alone;
+    GQA with 4 query heads per KV head. Compared in full."""
+    torch = require_gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hkv = sms // 2 if sms % 2 == 0 else sms
+    Hq, S, d = 2 * sms, 640, 128
+    n_qp = -(-S // 256)
+    items = Hq * ((n_qp + 1) // 2)
+    assert n_qp % 2 == 1 and items >= 4 * sms  # the pair-order branch of the launch
+    q, k, v = inputs.draw_qkv_bf16(1, Hq, Hkv, S, S, d, seed=640 + causal)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_bf16(torch, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
+                                         inputs.bf16_bits(v), causal, scale)
+    st = assert_o_close(o, o_ref)
+    record(f"pair order b1hq{Hq}hkv{Hkv}s{S}{'c' if causal else ''} (full)", "bf16", st,
+           assert_lse_close(lse, lse_ref), Hq * S)
 
 
 # ------------------------------------------------------------ fp16 inputs --
@@ -148,25 +198,19 @@ def test_f16_small_full_compare(oracle_mod, shape):
     assert o.dtype == torch.float16
     o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
                                          causal, scale, dtype="f16")
-    assert_o_close(o.float().cpu().numpy(), o_ref, kind="f16")
-    assert_lse_close(lse.cpu().numpy(), lse_ref)
+    st = assert_o_close(o.float().cpu().numpy(), o_ref, kind="f16")
+    record("small f16 b{}hq{}hkv{}sq{}sk{}d{}{}".format(*shape[:6], "c" if causal else ""), "f16",
+           st, assert_lse_close(lse.cpu().numpy(), lse_ref), B * Hq * Sq)
 
 
 @pytest.mark.gpu
-def test_f16_full_size_sampled_rows(oracle_mod):
-    torch = require_gpu()
+def test_f16_full_size_every_tile(oracle_mod):
     w = inputs.WORKLOADS["f16_b2h32s8192d128_causal"]
-    q, k, v = inputs.draw_workload_16(w)
-    o, lse = ea.forward(q.cuda(), k.cuda(), v.cuda(), causal=w.causal, scale=w.scale)
-    assert ea.attn_device_status() == ea.ATTN_OK
-    rows = inputs.sample_rows(w.B, w.Hq, w.Sq, 1200, seed=w.seed)
-    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(q), inputs.bits16(k), inputs.bits16(v),
-                                         w.causal, w.scale, dtype="f16", rows=rows)
-    b, rem = np.divmod(rows, w.Hq * w.Sq)
-    h, i = np.divmod(rem, w.Sq)
-    o_g = o[torch.as_tensor(b), torch.as_tensor(i), torch.as_tensor(h)].float().cpu().numpy()
-    assert_o_close(o_g, o_ref, kind="f16")
-    assert_lse_close(lse.cpu().numpy()[b, h, i], lse_ref)
+    torch, q, k, v, o, lse = _run_workload(w)
+    assert o.dtype == torch.float16
+    rows = inputs.stratified_rows(w.B, w.Hq, w.Sq, 128, seed=w.seed)
+    _compare_rows(oracle_mod, torch, w, q, k, v, o, lse, rows, w.name + " (every Q tile)",
+                  kind="f16")
 
 
 # ------------------------------------------------------------- large sizes --
