@@ -206,6 +206,43 @@ __device__ __forceinline__ void issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint3
   issue_pv_half<D, FP8, F16>(d_tmem, p_tmem, v_smem, 1, true);
 }
 
+// Warp-collective forms used by the kernel's MMA warp: the whole warp runs
+// them with the same operands and one elected lane issues each instruction.
+// The operand descriptors are formed once per tile (a_desc, b_desc: the
+// tile's first byte); each K step adds a compile-time byte offset to the
+// start-address field. Keeping the issue loop to a few uniform instructions
+// per MMA matters: the MMA warp shares its SM sub-partition with two softmax
+// warps, and an issue path of a dozen scalar instructions per MMA made issue,
+// not execution, the pace of the tensor pipe.
+template <int D, bool FP8, bool F16 = false>
+__device__ __forceinline__ void issue_qk_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc) {
+  using C = Cfg<D, FP8, F16>;
+#pragma unroll
+  for (int ks = 0; ks < C::KSTEPS_QK; ++ks) {
+    const uint32_t byte_k = ks * 32;
+    const uint32_t chunk = byte_k / C::CHUNK_BYTES;
+    const uint32_t within = byte_k % C::CHUNK_BYTES;
+    const uint64_t a = sdesc_add(a_desc, chunk * C::Q_CHUNK_BYTES + within);
+    const uint64_t b = sdesc_add(b_desc, chunk * C::KV_CHUNK_BYTES + within);
+    if constexpr (FP8) mma_f8_ss_w(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
+    else mma_f16_ss_w(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
+  }
+}
+
+template <int D, bool FP8, bool F16 = false>
+__device__ __forceinline__ void issue_pv_half_w(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
+                                                int half, bool accumulate) {
+  using C = Cfg<D, FP8, F16>;
+  constexpr int KS_HALF = C::KSTEPS_PV / 2;
+#pragma unroll
+  for (int k = 0; k < KS_HALF; ++k) {
+    const int ks = half * KS_HALF + k;
+    const uint64_t b = sdesc_add(v_desc, ks * 16 * C::V_CHUNK_BYTES);
+    const uint32_t a = p_tmem + ks * C::P_COLS_PER_KSTEP;
+    mma_f16_ts_w(d_tmem, a, b, C::IDESC_PV, (accumulate || ks > 0) ? 1u : 0u);
+  }
+}
+
 struct Unit {
   int b, hq, hkv, row0;
   int split, j0;  // key range: K/V tiles j0 + [0, n[t])
@@ -449,94 +486,102 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
     __syncwarp();
   } else if (warp == WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t it = 0, qit = 0;
-      uint32_t pc[2] = {0u, 0u};
-      bool ok = true;
-      const uint32_t q_smem = sbase + C::OFF_Q;
-      const uint32_t kv_smem = sbase + C::OFF_KV;
-
-      auto issue_s = [&](int t, uint32_t slot) {
-        issue_qk<D, FP8, F16>(tmem + C::COL_S0 + t * BN, q_smem + t * C::Q_TILE_BYTES,
-                         kv_smem + slot * C::KV_TILE_BYTES);
-      };
-      // V operand of O += P V: the staged tile, or (FP8) its widened copy
-      auto issue_o = [&](int t, uint32_t v_smem, int half, bool acc) {
-        issue_pv_half<D, FP8, F16>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN, v_smem,
+    // The whole warp runs this loop (warp-uniform control flow, so the loop
+    // state and the operand descriptors stay in uniform registers); one
+    // elected lane issues every tcgen05.mma and tcgen05.commit.
+    uint32_t it = 0, qit = 0;
+    uint32_t pc[2] = {0u, 0u};
+    bool ok = true;
+    // descriptors of Q tile 0 and of K/V slot 0 (K-major, as staged by TMA),
+    // and of the V operand of slot 0 or (FP8) of widened buffer 0 (MN-major)
+    const uint64_t q_desc = make_sdesc(sbase + C::OFF_Q, 16, 8 * C::CHUNK_BYTES, C::SWZ_CODE);
+    const uint64_t k_desc = make_sdesc(sbase + C::OFF_KV, 16, 8 * C::CHUNK_BYTES, C::SWZ_CODE);
+    const uint64_t v_desc = make_sdesc(sbase + (FP8 ? C::OFF_VF : C::OFF_KV), C::V_KV_CHUNK_BYTES,
+                                       8 * C::V_CHUNK_BYTES, 2u);
+    // every lane waits; the warp proceeds only if all of them saw the phase
+    auto wait_w = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl, P));
+    };
+    auto issue_s = [&](int t, uint32_t slot) {
+      issue_qk_w<D, FP8, F16>(tmem + C::COL_S0 + t * BN,
+                              sdesc_add(q_desc, t * C::Q_TILE_BYTES),
+                              sdesc_add(k_desc, slot * C::KV_TILE_BYTES));
+    };
+    auto issue_o = [&](int t, uint64_t vd, int half, bool acc) {
+      issue_pv_half_w<D, FP8, F16>(tmem + C::COL_O0 + t * D, tmem + C::COL_S0 + t * BN, vd,
                                    half, acc);
-      };
+    };
 
-      for (int i = 0; ok; ++i) {
-        Unit U;
-        const int st = cta_unit(i, P, U);
-        if (st == 0) break;
-        if (st == 1 || U.nmax == 0) continue;
-        if (!wait_bounded(BAR_Q_FULL, qit & 1u, ctl, P)) { ok = false; break; }
+    for (int i = 0; ok; ++i) {
+      Unit U;
+      const int st = cta_unit(i, P, U);
+      if (st == 0) break;
+      if (st == 1 || U.nmax == 0) continue;
+      if (!wait_w(BAR_Q_FULL, qit & 1u)) { ok = false; break; }
+      tc_fence_after();
+      {
+        const uint32_t slot = it % C::NSLOT;
+        if (!wait_w(BAR_KV_FULL + 8 * slot, (it / C::NSLOT) & 1u)) { ok = false; break; }
         tc_fence_after();
-        {
-          const uint32_t slot = it % C::NSLOT;
-          if (!wait_bounded(BAR_KV_FULL + 8 * slot, (it / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
-          tc_fence_after();
 #pragma unroll
-          for (int t = 0; t < 2; ++t)
-            if (U.n[t] > 0) {
-              issue_s(t, slot);
-              tc_commit(BAR_S_FULL + 8 * t);
-            }
-          tc_commit(BAR_KV_EMPTY + 8 * slot);
-          if (U.nmax == 1) tc_commit(BAR_Q_EMPTY);
-        }
-        for (int j = 0; j < U.nmax; ++j) {
-          const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
-          const uint32_t itk = itv + 1, kslot = itk % C::NSLOT;
-          const bool more = j + 1 < U.nmax;
-          // FP8: the widening warps wait for the staged V tile; this thread
-          // waits for their fp16 copy (buffer = V use parity)
-          const uint32_t vuse = itv >> 1, vbuf = vuse & 1u;
-          const uint32_t v_smem = FP8 ? sbase + C::OFF_VF + vbuf * C::V16_TILE_BYTES
-                                      : kv_smem + vslot * C::KV_TILE_BYTES;
-          if (FP8) {
-            if (!wait_bounded(BAR_VF_FULL + 8 * vbuf, (vuse >> 1) & 1u, ctl, P)) { ok = false; break; }
-          } else {
-            if (!wait_bounded(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
+        for (int t = 0; t < 2; ++t)
+          if (U.n[t] > 0) {
+            issue_s(t, slot);
+            tc_commit_w(BAR_S_FULL + 8 * t);
           }
-          tc_fence_after();
-#pragma unroll
-          for (int t = 0; t < 2; ++t) {
-            if (j < U.n[t]) {
-              // P arrives in two halves of 64 keys, one barrier each
-              for (int h = 0; ok && h < 2; ++h) {
-                if (!wait_bounded(BAR_P_FULL + 16 * t + 8 * h, pc[t] & 1u, ctl, P)) { ok = false; break; }
-                tc_fence_after();
-                issue_o(t, v_smem, h, j > 0);
-              }
-              if (!ok) break;
-              ++pc[t];
-              if (j == U.n[t] - 1) tc_commit(BAR_O_FULL + 8 * t);
-            }
-            if (t == 0 && more) {
-              if (!wait_bounded(BAR_KV_FULL + 8 * kslot, (itk / C::NSLOT) & 1u, ctl, P)) { ok = false; break; }
-              tc_fence_after();
-            }
-            if (j + 1 < U.n[t]) {
-              issue_s(t, kslot);
-              tc_commit(BAR_S_FULL + 8 * t);
-            }
-          }
-          if (!ok) break;
-          tc_commit(FP8 ? BAR_VF_EMPTY + 8 * vbuf : BAR_KV_EMPTY + 8 * vslot);
-          if (more) {
-            tc_commit(BAR_KV_EMPTY + 8 * kslot);
-            if (j + 2 == U.nmax) tc_commit(BAR_Q_EMPTY);
-          }
-        }
-        it += 2 * U.nmax;
-        ++qit;
+        tc_commit_w(BAR_KV_EMPTY + 8 * slot);
+        if (U.nmax == 1) tc_commit_w(BAR_Q_EMPTY);
       }
-      // Drain: all issued MMAs complete before the tensor memory is freed.
-      tc_commit(BAR_DRAIN);
-      drain_wait(BAR_DRAIN, 0u, P);
+      for (int j = 0; j < U.nmax; ++j) {
+        const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
+        const uint32_t itk = itv + 1, kslot = itk % C::NSLOT;
+        const bool more = j + 1 < U.nmax;
+        // FP8: the widening warps wait for the staged V tile; this warp
+        // waits for their fp16 copy (buffer = V use parity)
+        const uint32_t vuse = itv >> 1, vbuf = vuse & 1u;
+        const uint64_t vd = FP8 ? sdesc_add(v_desc, vbuf * C::V16_TILE_BYTES)
+                                : sdesc_add(v_desc, vslot * C::KV_TILE_BYTES);
+        if (FP8) {
+          if (!wait_w(BAR_VF_FULL + 8 * vbuf, (vuse >> 1) & 1u)) { ok = false; break; }
+        } else {
+          if (!wait_w(BAR_KV_FULL + 8 * vslot, (itv / C::NSLOT) & 1u)) { ok = false; break; }
+        }
+        tc_fence_after();
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          if (j < U.n[t]) {
+            // P arrives in two halves of 64 keys, one barrier each
+            for (int h = 0; ok && h < 2; ++h) {
+              if (!wait_w(BAR_P_FULL + 16 * t + 8 * h, pc[t] & 1u)) { ok = false; break; }
+              tc_fence_after();
+              issue_o(t, vd, h, j > 0);
+            }
+            if (!ok) break;
+            ++pc[t];
+            if (j == U.n[t] - 1) tc_commit_w(BAR_O_FULL + 8 * t);
+          }
+          if (t == 0 && more) {
+            if (!wait_w(BAR_KV_FULL + 8 * kslot, (itk / C::NSLOT) & 1u)) { ok = false; break; }
+            tc_fence_after();
+          }
+          if (j + 1 < U.n[t]) {
+            issue_s(t, kslot);
+            tc_commit_w(BAR_S_FULL + 8 * t);
+          }
+        }
+        if (!ok) break;
+        tc_commit_w(FP8 ? BAR_VF_EMPTY + 8 * vbuf : BAR_KV_EMPTY + 8 * vslot);
+        if (more) {
+          tc_commit_w(BAR_KV_EMPTY + 8 * kslot);
+          if (j + 2 == U.nmax) tc_commit_w(BAR_Q_EMPTY);
+        }
+      }
+      it += 2 * U.nmax;
+      ++qit;
     }
+    // Drain: all issued MMAs complete before the tensor memory is freed.
+    tc_commit_w(BAR_DRAIN);
+    drain_wait(BAR_DRAIN, 0u, P);
     __syncwarp();
   } else if (FP8 && warp >= WARP_WIDEN) {
     // ------------------------------------------------ V widening (FP8 only)
