@@ -24,8 +24,8 @@ __all__ = [
     "attn_fwd", "attn_fwd_fp8", "attn_fwd_splitkv", "attn_fwd_splitkv_noalloc",
     "attn_splitkv_plan", "attn_qk_rmsnorm", "qk_rmsnorm", "attn_bwd", "attn_bwd_workspace_size",
     "backward",
-    "attn_quantize_fp8_e4m3", "attn_device_status",
-    "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
+    "attn_quantize_fp8_e4m3", "attn_device_status", "attn_set_wait_limit_ns",
+    "attn_get_wait_limit_ns", "attn_status_string", "forward", "forward_fp8", "forward_splitkv", "quantize_fp8",
     "library_path", "load",
 ]
 
@@ -92,6 +92,10 @@ def load():
         lib.attn_bwd_workspace_size.restype = I
         lib.attn_device_status.argtypes = [P]
         lib.attn_device_status.restype = I
+        lib.attn_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+        lib.attn_set_wait_limit_ns.restype = I
+        lib.attn_get_wait_limit_ns.argtypes = []
+        lib.attn_get_wait_limit_ns.restype = ctypes.c_ulonglong
         lib.attn_status_string.argtypes = [I]
         lib.attn_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -189,6 +193,14 @@ def attn_bwd_workspace_size(B, Hq, Sq):
 
 def attn_device_status(stream=None) -> int:
     return load().attn_device_status(_stream(stream))
+
+
+def attn_set_wait_limit_ns(ns: int) -> int:
+    return load().attn_set_wait_limit_ns(int(ns))
+
+
+def attn_get_wait_limit_ns() -> int:
+    return int(load().attn_get_wait_limit_ns())
 
 
 def attn_status_string(code: int) -> str:

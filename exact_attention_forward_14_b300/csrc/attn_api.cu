@@ -34,7 +34,13 @@ using attnb3::get_encoder;
 __device__ int g_attn_status = 0;
 
 constexpr int kMaxDevices = 64;
-constexpr unsigned long long kWaitLimitNs = 1000000000ull;  // 1 s per wait
+constexpr unsigned long long kWaitLimitDefaultNs = 1000000000ull;  // 1 s per wait
+constexpr unsigned long long kWaitLimitMinNs = 1000000ull;            // 1 ms
+constexpr unsigned long long kWaitLimitMaxNs = 3600000000000ull;      // 1 h
+// Limit of every bounded wait in the kernels, read at each launch.
+std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitDefaultNs};
+
+unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 constexpr int kMaxSplits = 256;  // key ranges per split-KV call
 
 struct DeviceInfo {
@@ -141,7 +147,7 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
   P.num_items = B * Hq * P.npair * P.nsplit;
   P.causal = causal ? 1 : 0;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  P.timeout_ns = kWaitLimitNs;
+  P.timeout_ns = wait_limit_ns();
   P.status = di->status;
 
   // fewer than 4 whole items per SM leave the last round part-empty: deal
@@ -205,7 +211,7 @@ int launch_d256(const void* q, const void* k, const void* v, void* o, float* lse
   P.nsplit = 1;
   P.kps = P.nkv;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-  P.timeout_ns = kWaitLimitNs;
+  P.timeout_ns = wait_limit_ns();
   P.status = di->status;
   const int grid = P.num_items < di->num_sms ? P.num_items : di->num_sms;
   kern<<<grid, attnb3::WIDE_THREADS, C::SMEM_ALLOC, stream>>>(tq, tk, tv, P);
@@ -332,7 +338,7 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
   P.q_items = B * Hq * P.q_npair;
   P.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   P.scale = scale;
-  P.timeout_ns = kWaitLimitNs;
+  P.timeout_ns = wait_limit_ns();
   P.status = di->status;
 
   // row statistics: warps over the rows in memory order (D / 8 lanes per row,
@@ -362,23 +368,23 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
 constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(64) << 20;  // 64 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// The array's device address, looked up once per device (with that device
-// current); in host code the array's name is only a stand-in for it.
-std::once_flag g_scratch_once[kMaxDevices];
+// The array's device address, looked up per device (with that device
+// current) until a lookup succeeds; in host code the array's name is only a
+// stand-in for it. A failed lookup is not cached, so a transient error does
+// not disable the entry point for the rest of the process.
+std::mutex g_scratch_mu;
 void* g_scratch_ptr[kMaxDevices];
-int g_scratch_rc[kMaxDevices];
 
 int noalloc_scratch(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return ATTN_ERR_CUDA;
-  std::call_once(g_scratch_once[dev], [dev] {
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
     void* ptr = nullptr;
-    g_scratch_rc[dev] = cudaGetSymbolAddress(&ptr, g_noalloc_scratch) == cudaSuccess
-                            ? ATTN_OK
-                            : ATTN_ERR_CUDA;
+    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr)
+      return ATTN_ERR_CUDA;
     g_scratch_ptr[dev] = ptr;
-  });
-  if (g_scratch_rc[dev] != ATTN_OK) return g_scratch_rc[dev];
+  }
   *out = g_scratch_ptr[dev];
   return ATTN_OK;
 }
@@ -490,6 +496,9 @@ int attn_fwd_splitkv_noalloc(const void* q, const void* k, const void* v, void* 
                              float scale, int dtype, int num_splits, attn_stream_t stream) {
   int rc = check_attn_args(q, k, v, o, lse, B, Hq, Hkv, Sq, Sk, d, scale);
   if (rc != ATTN_OK) return rc;
+  // the same type and size checks as attn_fwd_splitkv, in the same order, so
+  // both entry points return the same code for the same request
+  if (dtype != ATTN_BF16 && dtype != ATTN_F16) return ATTN_ERR_UNSUPPORTED;
   if (d == 256) return ATTN_ERR_UNSUPPORTED;
   if (num_splits < 1 || num_splits > kMaxSplits) return ATTN_ERR_INVALID_ARG;
   int kps = 0, nsplit = 0;
@@ -610,6 +619,14 @@ int attn_device_status(attn_stream_t stream) {
     return ATTN_ERR_CUDA;
   return v;
 }
+
+int attn_set_wait_limit_ns(unsigned long long ns) {
+  if (ns < kWaitLimitMinNs || ns > kWaitLimitMaxNs) return ATTN_ERR_INVALID_ARG;
+  g_wait_limit_ns.store(ns, std::memory_order_relaxed);
+  return ATTN_OK;
+}
+
+unsigned long long attn_get_wait_limit_ns(void) { return wait_limit_ns(); }
 
 const char* attn_status_string(int code) {
   switch (code) {

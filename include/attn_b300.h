@@ -55,8 +55,9 @@ typedef enum {
                                  not compute capability 10.3 (B300) */
     ATTN_ERR_MISALIGNED = 3,  /* a pointer not 16-byte aligned (TMA rule) */
     ATTN_ERR_CUDA = 4,        /* a CUDA runtime / driver call failed */
-    ATTN_ERR_TIMEOUT = 5      /* a kernel-internal wait gave up (watchdog);
-                                 reported by attn_device_status() only */
+    ATTN_ERR_TIMEOUT = 5      /* a kernel-internal wait gave up (watchdog, see
+                                 attn_set_wait_limit_ns); reported by
+                                 attn_device_status() only */
 } attn_status_t;
 
 typedef enum {
@@ -160,8 +161,9 @@ int attn_fwd_splitkv(const void* q, const void* k, const void* v, void* o, float
  *   The workspace the call needs, num_splits' * B * Hq * Sq * (d + 1) * 4
  *   bytes (num_splits' = the non-empty ranges), must not exceed 64 MiB;
  *   larger requests return ATTN_ERR_INVALID_ARG without launching anything.
- *   The first call on a device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture.
+ *   The first successful call on a device (with that device current) looks
+ *   up the array's device address; make that first call before any stream
+ *   capture. A failed lookup is not cached: the next call tries again.
  *   Every call on a device shares the one array and it keeps the last call's
  *   contents; nothing in it needs clearing (each call writes every entry it
  *   reads), but calls whose kernels overlap on the GPU (other streams, other
@@ -259,6 +261,25 @@ int attn_bwd(const void* q, const void* k, const void* v, const void* o, const f
  * The word is shared by every launch on the current device.
  */
 int attn_device_status(attn_stream_t stream);
+
+/*
+ * attn_set_wait_limit_ns -- wall-clock limit of every bounded wait inside the
+ * tensor-core kernels (a wait on a shared-memory barrier for a copy, a matrix
+ * product or another warp). Default 1,000,000,000 (1 s). The limit is read
+ * when a kernel is launched, so it applies to calls enqueued after this one
+ * returns; it is process-wide (all devices, all threads).
+ * The waits measure wall time (the GPU's global timer), not the time the
+ * kernel actually ran: on a GPU shared with other contexts (time slicing,
+ * preemption, a debugger) a healthy launch can be descheduled for longer
+ * than the limit, and it then ends early with ATTN_ERR_TIMEOUT and undefined
+ * outputs. Callers on such GPUs should raise the limit.
+ *   ns : new limit, 1,000,000 (1 ms) .. 3,600,000,000,000 (1 h)
+ * Returns ATTN_OK, or ATTN_ERR_INVALID_ARG (limit unchanged) outside that range.
+ */
+int attn_set_wait_limit_ns(unsigned long long ns);
+
+/* attn_get_wait_limit_ns -- the limit currently in force, in nanoseconds. */
+unsigned long long attn_get_wait_limit_ns(void);
 
 /* attn_status_string -- static, human-readable name of a status code. */
 const char* attn_status_string(int code);

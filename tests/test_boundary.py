@@ -26,7 +26,8 @@ def lib():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return re.findall(r"^\s*(?:int|const char\s*\*)\s*(\w+)\s*\(", text, flags=re.M)
+    return re.findall(r"^\s*(?:int|const char\s*\*|unsigned long long)\s*(\w+)\s*\(", text,
+                      flags=re.M)
 
 
 def test_header_declares_the_boundary():
@@ -44,6 +45,23 @@ def test_watchdog_test_library_exports_the_same_boundary(lib):
     wd = ctypes.CDLL(os.path.join(PKG, "libattn_watchdog_test.so"))
     for name in declared_functions():
         assert hasattr(wd, name), name
+
+
+def test_wait_limit_is_settable_within_its_range(lib):
+    default = ea.attn_get_wait_limit_ns()
+    assert default == 1_000_000_000
+    try:
+        assert ea.attn_set_wait_limit_ns(5_000_000_000) == ea.ATTN_OK
+        assert ea.attn_get_wait_limit_ns() == 5_000_000_000
+        # out of range: rejected, limit unchanged
+        assert ea.attn_set_wait_limit_ns(999_999) == ea.ATTN_ERR_INVALID_ARG
+        assert ea.attn_set_wait_limit_ns(3_600_000_000_001) == ea.ATTN_ERR_INVALID_ARG
+        assert ea.attn_set_wait_limit_ns(0) == ea.ATTN_ERR_INVALID_ARG
+        assert ea.attn_get_wait_limit_ns() == 5_000_000_000
+        assert ea.attn_set_wait_limit_ns(1_000_000) == ea.ATTN_OK
+        assert ea.attn_set_wait_limit_ns(3_600_000_000_000) == ea.ATTN_OK
+    finally:
+        assert ea.attn_set_wait_limit_ns(default) == ea.ATTN_OK
 
 
 def test_status_strings(lib):
@@ -256,6 +274,28 @@ def test_d256_is_forward_only(lib):
                        1, 0.1, ea.ATTN_BF16, 0xC0000, 1 << 20, stream=0) == ea.ATTN_ERR_UNSUPPORTED
     assert ea.attn_fwd(Q, K, V, O, L, 1, 2, 2, 64, 64, 192, 1, 0.1, ea.ATTN_BF16,
                        stream=0) == ea.ATTN_ERR_UNSUPPORTED
+
+
+def test_noalloc_checks_match_the_workspace_entry_point(lib):
+    """attn_fwd_splitkv_noalloc returns the codes attn_fwd_splitkv returns for
+    the same request, and checks the type before its array's size (an
+    oversized E4M3 request is unsupported, not too large); all on the host."""
+    big = dict(B=4, Hq=64, Sq=2048, Sk=32768)  # 69 GB of workspace at 256 ranges
+    for dtype, d, splits, code in [(ea.ATTN_FP8_E4M3, 128, 256, ea.ATTN_ERR_UNSUPPORTED),
+                                   (7, 128, 2, ea.ATTN_ERR_UNSUPPORTED),
+                                   (ea.ATTN_BF16, 256, 2, ea.ATTN_ERR_UNSUPPORTED),
+                                   (ea.ATTN_BF16, 128, 0, ea.ATTN_ERR_INVALID_ARG),
+                                   (ea.ATTN_BF16, 128, 257, ea.ATTN_ERR_INVALID_ARG),
+                                   (ea.ATTN_BF16, 128, 256, ea.ATTN_ERR_INVALID_ARG)]:
+        Sk = big["Sk"] if d == 128 else 1024  # d = 256: every tensor below 2^31 elements
+        rc = ea.attn_fwd_splitkv_noalloc(Q, K, V, O, L, big["B"], big["Hq"], big["Hq"],
+                                         big["Sq"], Sk, d, 0, 0.1, dtype, splits, stream=0)
+        assert rc == code, (dtype, d, splits, rc)
+        if splits != 256 or dtype != ea.ATTN_BF16:  # the workspace form has no size to refuse
+            rc2 = ea.attn_fwd_splitkv(Q, K, V, O, L, big["B"], big["Hq"], big["Hq"], big["Sq"],
+                                      Sk, d, 0, 0.1, dtype, splits, 0x60000, 1 << 62,
+                                      stream=0)
+            assert rc2 == code, (dtype, d, splits, rc2)
 
 
 def test_bwd_rejects_padded_row_statistics_past_32_bits(lib):

@@ -3,12 +3,20 @@
 It exists for callers that may not allocate device memory themselves (a
 plugin inside an application that owns all device buffers, or a loop that must
 not call cudaMalloc / cudaFree). Its workspace is a fixed 64 MiB array inside
-the library. Here it is called through the C ABI and compared with the
-regular attn_fwd_splitkv, which is given a workspace allocated by the test, on
-two calls in a row with different shapes. The second call reuses the array
-the first one filled. This file is collected last, so that a run stopping at
-its first failure has already run every other test. It also passes on its
-own in a fresh process: the first call does the per-device set-up.
+the library. Here it is called through the C ABI, several times in a row, and
+each result is checked twice:
+  * bit for bit against the regular attn_fwd_splitkv given a workspace the test
+    allocates: both run the same kernels with the same split on the same
+    inputs, so any difference is a fault of the built-in array (a wrong offset,
+    or stale data a call read instead of writing);
+  * element by element against the fp64 oracle.
+The first two calls have the same shape, non-causal then causal, so the causal
+call uses exactly the array entries the non-causal one filled; under the
+causal mask the later key ranges are empty for the early query rows, and the
+merge is right only if the call wrote those ranges' entries itself. This file
+is collected last, so a run stopping at its first failure has already run
+every other test. It also passes on its own in a fresh process: the first
+call does the per-device set-up.
 """
 import numpy as np
 import pytest
@@ -19,14 +27,17 @@ from tests.helpers import assert_lse_close, assert_o_close, require_gpu
 
 # (B, Hq, Hkv, Sq, Sk, d, causal, dtype, num_splits)
 CALLS = [
-    (1, 8, 2, 64, 5000, 128, False, "bf16", 7),
+    (1, 4, 2, 1000, 1024, 128, False, "bf16", 8),
+    (1, 4, 2, 1000, 1024, 128, True, "bf16", 8),
     (2, 4, 4, 300, 3000, 64, True, "f16", 5),
+    (1, 8, 2, 64, 5000, 128, False, "bf16", 7),
 ]
 
 
-def _both(torch, B, Hq, Hkv, Sq, Sk, d, causal, dtype, num_splits, seed):
+def _call(oracle_mod, torch, B, Hq, Hkv, Sq, Sk, d, causal, dtype, num_splits, seed):
     draw = inputs.draw_qkv_f16 if dtype == "f16" else inputs.draw_qkv_bf16
-    q, k, v = (t.cuda() for t in draw(B, Hq, Hkv, Sq, Sk, d, seed=seed))
+    qh, kh, vh = draw(B, Hq, Hkv, Sq, Sk, d, seed=seed)
+    q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
     code = ea.ATTN_F16 if dtype == "f16" else ea.ATTN_BF16
     scale = 1.0 / np.sqrt(d)
     o = torch.empty((B, Sq, Hq, d), dtype=q.dtype, device="cuda")
@@ -35,20 +46,22 @@ def _both(torch, B, Hq, Hkv, Sq, Sk, d, causal, dtype, num_splits, seed):
                                      num_splits)
     assert rc == ea.ATTN_OK, ea.attn_status_string(rc)
     assert ea.attn_device_status() == ea.ATTN_OK
-    o_ref, lse_ref = ea.forward_splitkv(q, k, v, causal=causal, scale=scale,
-                                        num_splits=num_splits)
+    # the same request with a workspace of the test's own
+    o_ws, lse_ws = ea.forward_splitkv(q, k, v, causal=causal, scale=scale, num_splits=num_splits)
     assert ea.attn_device_status() == ea.ATTN_OK
-    return o, lse, o_ref, lse_ref
+    assert torch.equal(o, o_ws), "O differs from attn_fwd_splitkv"
+    assert torch.equal(lse, lse_ws), "LSE differs from attn_fwd_splitkv"
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bits16(qh), inputs.bits16(kh), inputs.bits16(vh),
+                                         causal, scale, dtype=dtype)
+    assert_o_close(o.float().cpu().numpy(), o_ref, kind=dtype)
+    assert_lse_close(lse.cpu().numpy(), lse_ref)
 
 
 @pytest.mark.gpu
-def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
+def test_noalloc_is_bit_identical_to_the_workspace_entry_point_and_matches_the_oracle(oracle_mod):
     torch = require_gpu()
     for i, call in enumerate(CALLS):
-        o, lse, o_ref, lse_ref = _both(torch, *call, seed=300 + i)
-        kind = call[7]
-        assert_o_close(o.float().cpu().numpy(), o_ref.float().cpu().numpy(), kind=kind)
-        assert_lse_close(lse.cpu().numpy(), lse_ref.cpu().numpy())
+        _call(oracle_mod, torch, *call, seed=300 + i)
 
 
 @pytest.mark.gpu
@@ -62,4 +75,8 @@ def test_noalloc_rejects_a_workspace_beyond_its_array():
     rc = ea.attn_fwd_splitkv_noalloc(x, x, x, x, lse, B, Hq, Hq, Sq, Sk, d, False, 0.1,
                                      ea.ATTN_BF16, 256)
     assert rc == ea.ATTN_ERR_INVALID_ARG
+    # an E4M3 request is unsupported whatever its size, as for attn_fwd_splitkv
+    rc = ea.attn_fwd_splitkv_noalloc(x, x, x, x, lse, B, Hq, Hq, Sq, Sk, d, False, 0.1,
+                                     ea.ATTN_FP8_E4M3, 256)
+    assert rc == ea.ATTN_ERR_UNSUPPORTED
     assert ea.attn_device_status() == ea.ATTN_OK
