@@ -11,9 +11,10 @@ causal. Workloads named ``bwd_*`` time the backward pass instead (one
 ``attn_bwd`` call: dQ, dK, dV from q, k, v, O, LSE and dO), counted as 2.5
 times the forward's FLOPs. Prints ONE JSON line on rank 0.
 
-With N > 1 (one process per GPU, launched by torch.distributed.run) every rank
-runs the same workload on its own GPU (independent replicas: the heads of
-the batch are independent, nothing is exchanged), timing is bracketed by
+With N > 1 (one process per GPU, launched by torch.distributed.run; given
+--gpus N outside such a launch, the script starts the N ranks itself) every
+rank runs the same workload on its own GPU (independent replicas: the heads
+of the batch are independent, nothing is exchanged), timing is bracketed by
 barriers, the time is the max over ranks and ``value`` counts all ranks' work.
 
 ``--impl reference`` times the CPU oracle (fp64, the host's cores) on a
@@ -171,6 +172,88 @@ class ClockSampler:
         return out
 
 
+class NvmlClockSampler:
+    """Samples the SM clock, power and clock-event reasons through NVML from a
+    background thread every ~1 ms while the timed region runs, so even a
+    region of a few milliseconds gets samples (nvidia-smi's loop cannot go
+    much below 20 ms). Same interface as ClockSampler, which is the fallback
+    when NVML is unavailable."""
+
+    def __init__(self, device_index: int, period_s: float = 0.001):
+        self.period_s = period_s
+        self.index = ClockSampler(device_index).index
+        self.rows = []  # (sm_mhz, max_mhz, watts, reasons bitmask)
+        self.error = None
+        self._nvml = None
+        self._h = None
+        self._thread = None
+        self._stop = threading.Event()
+        self._active = False
+
+    def start(self):
+        try:
+            import pynvml
+            pynvml.nvmlInit()
+            self._nvml = pynvml
+            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
+            self._max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
+        except Exception as e:  # NVML missing or refused: the caller falls back
+            self.error = f"{type(e).__name__}: {e}"
+            self._nvml = None
+            return self
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+        return self
+
+    def _loop(self):
+        n = self._nvml
+        while not self._stop.is_set():
+            if self._active:
+                try:
+                    self.rows.append((
+                        float(n.nvmlDeviceGetClockInfo(self._h, n.NVML_CLOCK_SM)), self._max,
+                        n.nvmlDeviceGetPowerUsage(self._h) / 1000.0,
+                        int(n.nvmlDeviceGetCurrentClocksEventReasons(self._h))))
+                except Exception as e:
+                    self.error = f"{type(e).__name__}: {e}"
+            time.sleep(self.period_s)
+
+    def __enter__(self):
+        self._active = True
+        return self
+
+    def __exit__(self, *exc):
+        self._active = False
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        n = self._nvml
+        bits = {} if n is None else {
+            "hw_slowdown": n.nvmlClocksEventReasonHwSlowdown,
+            "hw_thermal_slowdown": n.nvmlClocksEventReasonHwThermalSlowdown,
+            "sw_thermal_slowdown": n.nvmlClocksEventReasonSwThermalSlowdown,
+            "sw_power_cap": n.nvmlClocksEventReasonSwPowerCap,
+            "hw_power_brake_slowdown": n.nvmlClocksEventReasonHwPowerBrakeSlowdown}
+        reasons = sorted({name for *_, r in self.rows for name, b in bits.items() if r & b})
+        mhz = [r[0] for r in self.rows]
+        out = {"sm_mhz": statistics.median(mhz) if mhz else None,
+               "sm_max_mhz": max(r[1] for r in self.rows) if mhz else None,
+               "power_w_max": max(r[2] for r in self.rows) if mhz else None,
+               "reasons": reasons, "samples": len(mhz),
+               "source": f"NVML, every {self.period_s * 1e3:g} ms"}
+        if self.error:
+            out["error"] = self.error
+        return out
+
+
+def clock_sampler(device_index: int):
+    """NVML sampler when NVML answers, else the nvidia-smi one."""
+    s = NvmlClockSampler(device_index).start()
+    return s if s._nvml is not None else ClockSampler(device_index).start()
+
+
 # ------------------------------------------------------------ CPU oracle --
 
 def _oracle_inputs(w):
@@ -249,11 +332,27 @@ def cpu_baseline(w, target_s: float = 12.0):
                          if w.backward else "fp64 two-pass oracle, OpenMP")}
 
 
+def count_ranks(backend: str = "gloo") -> int:
+    """Number of ranks that joined this job (1 without torch.distributed):
+    every rank adds 1 in an all-reduce. Leaves no process group behind."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world == 1:
+        return 1
+    import torch
+    import torch.distributed as dist
+    dist.init_process_group(backend)
+    t = torch.ones(1, dtype=torch.int64)
+    dist.all_reduce(t)
+    dist.destroy_process_group()
+    return int(t.item())
+
+
 def run_reference(args, w):
     rank = int(os.environ.get("RANK", "0"))
+    ranks = count_ranks()  # every rank joins, so n_gpus counts the ranks that ran
     if rank != 0:
         return 0
-    per_step = max(0.5, 150.0 / (args.steps + args.warmup))
+    per_step = max(0.05, args.ref_seconds / (args.steps + args.warmup))
     bits = _oracle_inputs(w)
     _, _, n_step, _ = _oracle_sample(w, bits, per_step, seed=99)  # calibrate the step size
     flops_t = []
@@ -266,7 +365,7 @@ def run_reference(args, w):
     value = tot_f / tot_t / 1e12
     line = {
         "impl": "reference", "metric": metric_of(w), "value": value, "unit": "TFLOP/s",
-        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": ranks, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * tot_t / len(flops_t), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(w),
@@ -369,9 +468,11 @@ def mufu_ex2_rate(w, num_sms: int, sm_mhz: float):
             return None
     rates = [1024 * 8 * iters / c for c in cyc.cpu().tolist() if c > 0]
     rate = st.median(rates)
-    ceiling = rate * num_sms * sm_mhz * 1e6 * 4 * w.d / 1e12
+    ceiling = None if not sm_mhz else rate * num_sms * sm_mhz * 1e6 * 4 * w.d / 1e12
     return {"ex2_per_clk_per_sm": rate, "implied_ceiling_tflops": ceiling,
-            "note": "one exp2 per score element against 4 d tensor FLOPs; "
+            "at_sm_mhz": sm_mhz,
+            "note": "one exp2 per score element against 4 d tensor FLOPs, at the SM clock "
+                    "sampled in the timed region (null when no sample arrived); "
                     "microbenchmark in csrc/mufu_rate.cu"}
 
 
@@ -454,7 +555,7 @@ def gemm_peaks(n: int = 8192, reps: int = 40):
                                                    use_fast_accum=True),
     }
     out = {"n": n, "reps": reps}
-    clocks = ClockSampler(0).start()
+    clocks = clock_sampler(0)
     with clocks:
         for name, f in calls.items():
             for _ in range(5):
@@ -481,6 +582,11 @@ def run_ours(args, w):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world != args.gpus:
+        raise SystemExit(f"--gpus {args.gpus} but {world} rank(s) were launched")
+    if local >= torch.cuda.device_count():
+        raise SystemExit(f"rank {rank}: local rank {local} but only "
+                         f"{torch.cuda.device_count()} visible GPU(s)")
     dist = None
     if world > 1:
         import torch.distributed as dist
@@ -612,7 +718,7 @@ def run_ours(args, w):
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize(dev)
-    clocks = ClockSampler(local).start()
+    clocks = clock_sampler(local)
     with clocks:
         t0.record(stream)
         for i, (a, b) in enumerate(ev):
@@ -738,14 +844,29 @@ def run_ours(args, w):
                             "hbm_gbs": (in_b + out_b) / (med * 1e-3) / 1e9}
     if not w.backward:
         props = torch.cuda.get_device_properties(dev)
-        clk = line["clocks"].get("sm_mhz") or 2032.0
-        line["mufu"] = mufu_ex2_rate(w, props.multi_processor_count, float(clk))
+        # the ceiling uses the clock sampled in the timed region; none without samples
+        line["mufu"] = mufu_ex2_rate(w, props.multi_processor_count, line["clocks"].get("sm_mhz"))
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w)
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def launch_ranks(n: int, argv) -> int:
+    """Re-runs this script as n ranks on this node (one per GPU) through
+    torch.distributed.run, rendezvous on 127.0.0.1; returns their exit code.
+    Used when --gpus N > 1 is given outside a torchrun launch."""
+    import socket
+    import subprocess
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1",
+           f"--nproc-per-node={n}", "--master-addr=127.0.0.1", f"--master-port={port}",
+           os.path.abspath(__file__), *argv]
+    return subprocess.run(cmd).returncode
 
 
 def main(argv=None):
@@ -760,7 +881,12 @@ def main(argv=None):
                     help="skip the CPU oracle timing (e.g. under a profiler)")
     ap.add_argument("--gemm-peaks", action="store_true",
                     help="only time library bf16 and FP8 GEMMs (8192^3) and exit")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="--impl reference: seconds of oracle work over all steps (bounded sample)")
     args = ap.parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # N replicas need N processes: start them here rather than run one
+        return launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
     if args.gemm_peaks:
         return gemm_peaks()
     from exact_attention_forward_14_b300 import inputs

@@ -1,6 +1,8 @@
 """Host-side multi-rank logic of bench.py on CPU with the gloo backend and
 two ranks: the timed region's figure is the max over ranks, the job value
-counts every rank's work, and the reference arm does its work on rank 0 only."""
+counts every rank's work, and ``bench.py --gpus 2`` outside a torchrun launch
+starts two ranks itself (checked through the reference arm, which runs on the
+CPU: both ranks join, rank 0 alone does the oracle work and prints)."""
 import os
 import socket
 import sys
@@ -27,15 +29,9 @@ def _rank_main(rank, world, port, out):
     local_ms = 10.0 + 5.0 * rank  # rank 1 is the slow one
     got = bench.max_over_ranks(local_ms, dist, "cpu")
     value = bench.job_tflops(2.0e12, 4, world, got)
-    # the reference arm: ranks other than 0 return at once, without work
-    ref_rc = None
-    if rank != 0:
-        class A:  # the arguments run_reference reads
-            steps, warmup, gpus = 1, 0, world
-        ref_rc = bench.run_reference(A, None)
     dist.barrier()
     dist.destroy_process_group()
-    out.put((rank, got, value, ref_rc))
+    out.put((rank, got, value))
 
 
 def test_two_gloo_ranks_take_the_max_and_count_all_work():
@@ -49,11 +45,28 @@ def test_two_gloo_ranks_take_the_max_and_count_all_work():
     for p in procs:
         p.join(timeout=60)
         assert p.exitcode == 0
-    for rank, got, value, ref_rc in res:
+    for rank, got, value in res:
         assert got == 15.0
         # 2 ranks x 4 steps x 2e12 FLOP in 15 ms
         assert value == pytest.approx(2 * 4 * 2.0e12 / 15e-3 / 1e12)
-    assert res[1][3] == 0
+
+
+def test_gpus_2_starts_two_ranks_itself():
+    import json
+    import subprocess
+    env = dict(os.environ)
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK", "MASTER_ADDR", "MASTER_PORT"):
+        env.pop(k, None)
+    env["OMP_NUM_THREADS"] = "2"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2",
+                        "--impl", "reference", "--workload", "tiny_b1h1s128d64", "--steps", "2",
+                        "--warmup", "1", "--ref-seconds", "1.5"],
+                       capture_output=True, text=True, timeout=300, env=env, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout  # rank 0 alone prints
+    line = json.loads(lines[0])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["steps"] == 2
 
 
 def test_single_rank_is_identity():
