@@ -188,18 +188,23 @@ __device__ __forceinline__ uint32_t pack16x2(bool f16, float lo, float hi) {
 
 // ------------------------------------------------------------ MMA helpers --
 
+// Both helpers are warp-collective: the MMA warp runs them with the same
+// operands in every lane and one elected lane issues each instruction. The
+// operand descriptors are formed once per call, and each K step adds a
+// constant to the start-address field (as in the forward kernel's MMA warp).
+
 // D[tmem] = A * B^T with A and B two 128-row tiles (K-major, in 64-column
 // swizzled chunks of 128 rows); M = N = 128, K = d.
 template <int D, bool F16>
 __device__ __forceinline__ void issue_s128(uint32_t d_tmem, uint32_t a_smem, uint32_t b_smem) {
   using C = BwdCfg<D, F16>;
+  const uint64_t a0 = make_sdesc(a_smem, 16, 8 * C::CHUNK, 2u);
+  const uint64_t b0 = make_sdesc(b_smem, 16, 8 * C::CHUNK, 2u);
 #pragma unroll
   for (int ks = 0; ks < C::KSTEPS_D; ++ks) {
     const uint32_t byte_k = ks * 32;
     const uint32_t off = (byte_k / C::CHUNK) * C::CH + byte_k % C::CHUNK;
-    const uint64_t a = make_sdesc(a_smem + off, 16, 8 * C::CHUNK, 2u);
-    const uint64_t b = make_sdesc(b_smem + off, 16, 8 * C::CHUNK, 2u);
-    mma_f16_ss(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
+    mma_f16_ss_w(d_tmem, sdesc_add(a0, off), sdesc_add(b0, off), C::IDESC_S, ks > 0 ? 1u : 0u);
   }
 }
 
@@ -210,12 +215,11 @@ template <int D, bool F16>
 __device__ __forceinline__ void issue_acc64(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_smem,
                                             uint32_t b_chunk, int b_row0, bool accumulate) {
   using C = BwdCfg<D, F16>;
+  const uint64_t b0 = make_sdesc(b_smem + b_row0 * C::CHUNK, b_chunk, 8 * C::CHUNK, 2u);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {  // 16 rows of K per instruction
-    const uint64_t b =
-        make_sdesc(b_smem + (b_row0 + 16 * k) * C::CHUNK, b_chunk, 8 * C::CHUNK, 2u);
-    mma_f16_ts(d_tmem, a_tmem + 8 * k, b, C::IDESC_ACC, (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < 4; ++k)  // 16 rows of K per instruction
+    mma_f16_ts_w(d_tmem, a_tmem + 8 * k, sdesc_add(b0, 16 * k * C::CHUNK), C::IDESC_ACC,
+                 (accumulate || k > 0) ? 1u : 0u);
 }
 
 // ------------------------------------------------------------------ prep --
@@ -459,30 +463,35 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // dS(t) while they run dV(t) and S^T(t+1). The first products of a unit
     // overwrite dV and dK; they wait for p_full of that unit, which both
     // warpgroups arrive on only after their epilogue of the previous unit.
-    if (lane == 0) {
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues each tcgen05 instruction; every lane waits on the barriers.
+    {
+      auto bwait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, bwd_wait(bar, parity, ctl, P));
+      };
       uint32_t n = 0, u = 0, pc = 0, dc = 0;
       bool ok = true;
       const uint32_t k_s = sbase + C::KV_OFF_K, v_s = sbase + C::KV_OFF_V;
       auto wait_stage = [&](uint32_t nn) {
-        return bwd_wait(BAR_ST_FULL + 8 * (nn % C::NSTAGE), (nn / C::NSTAGE) & 1u, ctl, P);
+        return bwait(BAR_ST_FULL + 8 * (nn % C::NSTAGE), (nn / C::NSTAGE) & 1u);
       };
       for (int i = 0; ok; ++i) {
         KvUnit U;
         const int st = kv_unit(i, P, U);
         if (st == 0) break;
         if (st == 1 || U.T == 0) continue;
-        if (!bwd_wait(BAR_KV_FULL, u & 1u, ctl, P) || !wait_stage(n)) { ok = false; break; }
+        if (!bwait(BAR_KV_FULL, u & 1u) || !wait_stage(n)) { ok = false; break; }
         tc_fence_after();
         issue_s128<D, F16>(tmem + C::COL_ST, k_s, stage_smem(n));
-        tc_commit(BAR_S_FULL);
+        tc_commit_w(BAR_S_FULL);
         issue_s128<D, F16>(tmem + C::COL_DPT, v_s, stage_smem(n) + C::TILE);
-        tc_commit(BAR_DP_FULL);
+        tc_commit_w(BAR_DP_FULL);
         for (int t = 0; t < U.T; ++t) {
           const uint32_t nn = n + t;
           const uint32_t stg = stage_smem(nn);
           const bool more = t + 1 < U.T;
           const bool acc = t > 0;
-          if (!bwd_wait(BAR_P_FULL, pc & 1u, ctl, P)) { ok = false; break; }
+          if (!bwait(BAR_P_FULL, pc & 1u)) { ok = false; break; }
           ++pc;
           tc_fence_after();
 #pragma unroll
@@ -493,28 +502,28 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             if (!wait_stage(nn + 1)) { ok = false; break; }
             tc_fence_after();
             issue_s128<D, F16>(tmem + C::COL_ST, k_s, stage_smem(nn + 1));
-            tc_commit(BAR_S_FULL);
+            tc_commit_w(BAR_S_FULL);
           }
-          if (!bwd_wait(BAR_DS_FULL, dc & 1u, ctl, P)) { ok = false; break; }
+          if (!bwait(BAR_DS_FULL, dc & 1u)) { ok = false; break; }
           ++dc;
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             issue_acc64<D, F16>(tmem + C::COL_DK, tmem + C::COL_DPT + BWD_HALF * h, stg, C::CH,
                                 BWD_HALF * h, acc || h > 0);
-          tc_commit(BAR_ST_EMPTY + 8 * (nn % C::NSTAGE));
+          tc_commit_w(BAR_ST_EMPTY + 8 * (nn % C::NSTAGE));
           if (more) {
             issue_s128<D, F16>(tmem + C::COL_DPT, v_s, stage_smem(nn + 1) + C::TILE);
-            tc_commit(BAR_DP_FULL);
+            tc_commit_w(BAR_DP_FULL);
           }
         }
         if (!ok) break;
-        tc_commit(BAR_ACC_FULL);
-        tc_commit(BAR_KV_EMPTY);
+        tc_commit_w(BAR_ACC_FULL);
+        tc_commit_w(BAR_KV_EMPTY);
         n += U.T;
         ++u;
       }
-      tc_commit(BAR_DRAIN);
+      tc_commit_w(BAR_DRAIN);
       bwd_drain_wait(BAR_DRAIN, 0u, P);
     }
     __syncwarp();
@@ -819,13 +828,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     // while S(j+2) runs. In-order execution puts S(j+2) after dQ(j), which
     // reads dS(j) from the same buffer, and dP(j+1) after the element-wise
     // warps read dP(j) (ds_full). K_j is released after dQ(j), V_j after dP(j).
-    if (lane == 0) {
+    // The whole warp runs the loop (uniform control flow); one elected lane
+    // issues each tcgen05 instruction; every lane waits on the barriers.
+    {
+      auto bwait = [&](uint32_t bar, uint32_t parity) {
+        return __all_sync(0xffffffffu, bwd_wait(bar, parity, ctl, P));
+      };
       uint32_t it = 0, qit = 0, dsc = 0;
       bool ok = true;
       const uint32_t q_s = sbase + C::Q_OFF_Q, do_s = sbase + C::Q_OFF_DO;
       auto slot_smem = [&](uint32_t f) { return sbase + C::Q_OFF_KV + (f % C::NSLOT) * C::TILE; };
       auto wait_fill = [&](uint32_t f) {
-        return bwd_wait(BAR_KV_FULL + 8 * (f % C::NSLOT), (f / C::NSLOT) & 1u, ctl, P);
+        return bwait(BAR_KV_FULL + 8 * (f % C::NSLOT), (f / C::NSLOT) & 1u);
       };
       for (int i = 0; ok; ++i) {
         QUnit U;
@@ -833,54 +847,54 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         if (st == 0) break;
         if (st == 1 || U.n == 0) continue;
         const int n = U.n;
-        if (!bwd_wait(BAR_Q_FULL, qit & 1u, ctl, P) || !wait_fill(it) || !wait_fill(it + 1)) {
+        if (!bwait(BAR_Q_FULL, qit & 1u) || !wait_fill(it) || !wait_fill(it + 1)) {
           ok = false;
           break;
         }
         tc_fence_after();
         issue_s128<D, F16>(tmem + C::COL_SB0, q_s, slot_smem(it));
-        tc_commit(BAR_S_FULL);
+        tc_commit_w(BAR_S_FULL);
         issue_s128<D, F16>(tmem + C::COL_DP, do_s, slot_smem(it + 1));
-        tc_commit(BAR_DP_FULL);
-        tc_commit(BAR_KV_EMPTY + 8 * ((it + 1) % C::NSLOT));  // V_0
-        if (n == 1) tc_commit(BAR_Q_EMPTY);
+        tc_commit_w(BAR_DP_FULL);
+        tc_commit_w(BAR_KV_EMPTY + 8 * ((it + 1) % C::NSLOT));  // V_0
+        if (n == 1) tc_commit_w(BAR_Q_EMPTY);
         if (n > 1) {
           if (!wait_fill(it + 2)) { ok = false; break; }
           tc_fence_after();
           issue_s128<D, F16>(tmem + C::COL_SB1, q_s, slot_smem(it + 2));
-          tc_commit(BAR_S_FULL + 8);
+          tc_commit_w(BAR_S_FULL + 8);
         }
         for (int j = 0; j < n; ++j) {
           const uint32_t fk = it + 2 * j;  // fill of K_j; V_j is fk + 1
-          if (!bwd_wait(BAR_DS_FULL, dsc & 1u, ctl, P)) { ok = false; break; }
+          if (!bwait(BAR_DS_FULL, dsc & 1u)) { ok = false; break; }
           ++dsc;
           tc_fence_after();
 #pragma unroll
           for (int h = 0; h < 2; ++h)
             issue_acc64<D, F16>(tmem + C::COL_DQ, tmem + col_sbuf(j) + BWD_HALF * h,
                                 slot_smem(fk), C::CH, BWD_HALF * h, j > 0 || h > 0);
-          tc_commit(BAR_KV_EMPTY + 8 * (fk % C::NSLOT));  // K_j
+          tc_commit_w(BAR_KV_EMPTY + 8 * (fk % C::NSLOT));  // K_j
           if (j + 1 < n) {
             if (!wait_fill(fk + 3)) { ok = false; break; }
             tc_fence_after();
             issue_s128<D, F16>(tmem + C::COL_DP, do_s, slot_smem(fk + 3));
-            tc_commit(BAR_DP_FULL);
-            tc_commit(BAR_KV_EMPTY + 8 * ((fk + 3) % C::NSLOT));  // V_{j+1}
-            if (j + 2 == n) tc_commit(BAR_Q_EMPTY);  // dP(n-1) is the last reader of Q / dO
+            tc_commit_w(BAR_DP_FULL);
+            tc_commit_w(BAR_KV_EMPTY + 8 * ((fk + 3) % C::NSLOT));  // V_{j+1}
+            if (j + 2 == n) tc_commit_w(BAR_Q_EMPTY);  // dP(n-1) is the last reader of Q / dO
           }
           if (j + 2 < n) {
             if (!wait_fill(fk + 4)) { ok = false; break; }
             tc_fence_after();
             issue_s128<D, F16>(tmem + col_sbuf(j), q_s, slot_smem(fk + 4));
-            tc_commit(BAR_S_FULL + 8 * (j & 1));
+            tc_commit_w(BAR_S_FULL + 8 * (j & 1));
           }
         }
         if (!ok) break;
-        tc_commit(BAR_DQ_FULL);
+        tc_commit_w(BAR_DQ_FULL);
         it += 2 * n;
         ++qit;
       }
-      tc_commit(BAR_DRAIN);
+      tc_commit_w(BAR_DRAIN);
       bwd_drain_wait(BAR_DRAIN, 0u, P);
     }
     __syncwarp();

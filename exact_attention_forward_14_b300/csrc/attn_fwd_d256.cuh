@@ -105,32 +105,32 @@ __device__ __forceinline__ int wide_unit(int i, const FwdParams& P, WideUnit& U)
 }
 
 // S = Q K^T for the 128-row Q tile and one 64-key K tile (both K-major in
-// 64-column swizzled chunks); 32 bytes of d per instruction.
+// 64-column swizzled chunks); 32 bytes of d per instruction. Warp-collective:
+// the MMA warp runs it with descriptors of the tiles' first bytes, and each
+// K step adds a constant offset (see issue_qk_w).
 template <bool F16>
-__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint32_t q_smem, uint32_t k_smem) {
+__device__ __forceinline__ void wide_issue_s(uint32_t d_tmem, uint64_t q_desc, uint64_t k_desc) {
   using C = WideCfg<F16>;
 #pragma unroll
   for (int ks = 0; ks < WIDE_D / 16; ++ks) {
     const uint32_t byte_k = ks * 32;
     const uint32_t chunk = byte_k / C::CHUNK, within = byte_k % C::CHUNK;
-    const uint64_t a = make_sdesc(q_smem + chunk * C::Q_CH + within, 16, 8 * C::CHUNK, 2u);
-    const uint64_t b = make_sdesc(k_smem + chunk * C::KV_CH + within, 16, 8 * C::CHUNK, 2u);
-    mma_f16_ss(d_tmem, a, b, C::IDESC_S, ks > 0 ? 1u : 0u);
+    mma_f16_ss_w(d_tmem, sdesc_add(q_desc, chunk * C::Q_CH + within),
+                 sdesc_add(k_desc, chunk * C::KV_CH + within), C::IDESC_S, ks > 0 ? 1u : 0u);
   }
 }
 
 // O (+)= P V: P = 128 lanes x 64 keys packed in 32 TMEM columns, V = 64 keys
 // x 256 (d contiguous, MN-major, chunks KV_CH bytes apart); 16 keys per
-// instruction.
+// instruction. Warp-collective, v_desc describes the V tile's first byte.
 template <bool F16>
-__device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint32_t v_smem,
+__device__ __forceinline__ void wide_issue_pv(uint32_t d_tmem, uint32_t p_tmem, uint64_t v_desc,
                                               bool accumulate) {
   using C = WideCfg<F16>;
 #pragma unroll
-  for (int k = 0; k < WIDE_BN / 16; ++k) {
-    const uint64_t b = make_sdesc(v_smem + 16 * k * C::CHUNK, C::KV_CH, 8 * C::CHUNK, 2u);
-    mma_f16_ts(d_tmem, p_tmem + 8 * k, b, C::IDESC_PV, (accumulate || k > 0) ? 1u : 0u);
-  }
+  for (int k = 0; k < WIDE_BN / 16; ++k)
+    mma_f16_ts_w(d_tmem, p_tmem + 8 * k, sdesc_add(v_desc, 16 * k * C::CHUNK), C::IDESC_PV,
+                 (accumulate || k > 0) ? 1u : 0u);
 }
 
 template <bool F16>
@@ -233,62 +233,68 @@ __global__ void __launch_bounds__(WIDE_THREADS, 1)
   } else if (warp == WIDE_WARP_MMA) {
     // ------------------------------------------------------------ MMA issuer
     // K_j is released after S(j), V_j after PV(j); Q after the unit's last S.
-    if (lane == 0) {
-      uint32_t it = 0, qit = 0, pc[2] = {0u, 0u};
-      bool ok = true;
-      const uint32_t q_s = sbase + C::OFF_Q;
-      auto slot_smem = [&](uint32_t f) { return sbase + C::OFF_KV + (f % C::NSLOT) * C::KV_BYTES; };
-      auto wait_fill = [&](uint32_t f) {
-        return wait_bounded(BAR_KV_FULL + 8 * (f % C::NSLOT), (f / C::NSLOT) & 1u, ctl, P);
-      };
-      // S(j) into buffer j & 1; K_j is fill it + 2 j
-      auto issue_s = [&](int j) {
-        const uint32_t fk = it + 2 * j;
-        wide_issue_s<F16>(tmem + col_sbuf(j), q_s, slot_smem(fk));
-        tc_commit(BAR_S_FULL + 8 * (j & 1));
-        tc_commit(BAR_KV_EMPTY + 8 * (fk % C::NSLOT));
-      };
-      for (int i = 0; ok; ++i) {
-        WideUnit U;
-        const int st = wide_unit(i, P, U);
-        if (st == 0) break;
-        if (st == 1 || U.n == 0) continue;
-        const int n = U.n;
-        if (!wait_bounded(BAR_Q_FULL, qit & 1u, ctl, P) || !wait_fill(it)) { ok = false; break; }
+    // The whole warp runs the loop (uniform control flow and descriptors);
+    // one elected lane issues each tcgen05 instruction.
+    uint32_t it = 0, qit = 0, pc[2] = {0u, 0u};
+    bool ok = true;
+    const uint64_t q_desc = make_sdesc(sbase + C::OFF_Q, 16, 8 * C::CHUNK, 2u);
+    const uint64_t k_desc = make_sdesc(sbase + C::OFF_KV, 16, 8 * C::CHUNK, 2u);
+    const uint64_t v_desc = make_sdesc(sbase + C::OFF_KV, C::KV_CH, 8 * C::CHUNK, 2u);
+    auto slot_off = [&](uint32_t f) { return (f % C::NSLOT) * C::KV_BYTES; };
+    auto wait_w = [&](uint32_t bar, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_bounded(bar, parity, ctl, P));
+    };
+    auto wait_fill = [&](uint32_t f) {
+      return wait_w(BAR_KV_FULL + 8 * (f % C::NSLOT), (f / C::NSLOT) & 1u);
+    };
+    // S(j) into buffer j & 1; K_j is fill it + 2 j
+    auto issue_s = [&](int j) {
+      const uint32_t fk = it + 2 * j;
+      wide_issue_s<F16>(tmem + col_sbuf(j), q_desc, sdesc_add(k_desc, slot_off(fk)));
+      tc_commit_w(BAR_S_FULL + 8 * (j & 1));
+      tc_commit_w(BAR_KV_EMPTY + 8 * (fk % C::NSLOT));
+    };
+    for (int i = 0; ok; ++i) {
+      WideUnit U;
+      const int st = wide_unit(i, P, U);
+      if (st == 0) break;
+      if (st == 1 || U.n == 0) continue;
+      const int n = U.n;
+      if (!wait_w(BAR_Q_FULL, qit & 1u) || !wait_fill(it)) { ok = false; break; }
+      tc_fence_after();
+      issue_s(0);
+      if (n > 1) {
+        if (!wait_fill(it + 2)) { ok = false; break; }
         tc_fence_after();
-        issue_s(0);
-        if (n > 1) {
-          if (!wait_fill(it + 2)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(1);
-        }
-        if (n <= 2) tc_commit(BAR_Q_EMPTY);
-        for (int j = 0; j < n; ++j) {
-          const uint32_t fv = it + 2 * j + 1;  // fill of V_j
-          if (!wait_bounded(BAR_P_FULL + 8 * (j & 1), pc[j & 1] & 1u, ctl, P) || !wait_fill(fv)) {
-            ok = false;
-            break;
-          }
-          ++pc[j & 1];
-          tc_fence_after();
-          wide_issue_pv<F16>(tmem + C::COL_O, tmem + col_pbuf(j), slot_smem(fv), j > 0);
-          tc_commit(BAR_PV_DONE);
-          tc_commit(BAR_KV_EMPTY + 8 * (fv % C::NSLOT));
-          if (j + 2 < n) {
-            if (!wait_fill(it + 2 * (j + 2))) { ok = false; break; }
-            tc_fence_after();
-            issue_s(j + 2);
-            if (j + 3 == n) tc_commit(BAR_Q_EMPTY);  // S(n-1) was the last reader of Q
-          }
-        }
-        if (!ok) break;
-        tc_commit(BAR_O_FULL);
-        it += 2 * n;
-        ++qit;
+        issue_s(1);
       }
-      tc_commit(BAR_DRAIN);
-      drain_wait(BAR_DRAIN, 0u, P);
+      if (n <= 2) tc_commit_w(BAR_Q_EMPTY);
+      for (int j = 0; j < n; ++j) {
+        const uint32_t fv = it + 2 * j + 1;  // fill of V_j
+        if (!wait_w(BAR_P_FULL + 8 * (j & 1), pc[j & 1] & 1u) || !wait_fill(fv)) {
+          ok = false;
+          break;
+        }
+        ++pc[j & 1];
+        tc_fence_after();
+        wide_issue_pv<F16>(tmem + C::COL_O, tmem + col_pbuf(j), sdesc_add(v_desc, slot_off(fv)),
+                           j > 0);
+        tc_commit_w(BAR_PV_DONE);
+        tc_commit_w(BAR_KV_EMPTY + 8 * (fv % C::NSLOT));
+        if (j + 2 < n) {
+          if (!wait_fill(it + 2 * (j + 2))) { ok = false; break; }
+          tc_fence_after();
+          issue_s(j + 2);
+          if (j + 3 == n) tc_commit_w(BAR_Q_EMPTY);  // S(n-1) was the last reader of Q
+        }
+      }
+      if (!ok) break;
+      tc_commit_w(BAR_O_FULL);
+      it += 2 * n;
+      ++qit;
     }
+    tc_commit_w(BAR_DRAIN);
+    drain_wait(BAR_DRAIN, 0u, P);
     __syncwarp();
   } else if (warp < BM / 32) {
     // ------------------------------------------------------------- softmax
