@@ -169,53 +169,66 @@ class ClockSampler:
                "source": f"nvidia-smi -lms {self.period_ms}"}
         if self.error:
             out["error"] = self.error
+        if getattr(self, "nvml_error", None):
+            out["nvml_error"] = self.nvml_error
         return out
 
 
 class NvmlClockSampler:
-    """Samples the SM clock, power and clock-event reasons through NVML from a
-    background thread every ~1 ms while the timed region runs, so even a
-    region of a few milliseconds gets samples (nvidia-smi's loop cannot go
-    much below 20 ms). Same interface as ClockSampler, which is the fallback
-    when NVML is unavailable."""
+    """Samples the SM clock, power and clock-event reasons through NVML (the
+    driver's libnvidia-ml, called with ctypes) from a background thread every
+    ~1 ms while the timed region runs, so even a region of a few milliseconds
+    gets samples (nvidia-smi's loop cannot go much below 20 ms). Same
+    interface as ClockSampler, which is the fallback when NVML cannot be
+    loaded."""
+
+    NVML_CLOCK_SM = 1
+    # clock-event reason bits (nvml.h)
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
     def __init__(self, device_index: int, period_s: float = 0.001):
         self.period_s = period_s
         self.index = ClockSampler(device_index).index
         self.rows = []  # (sm_mhz, max_mhz, watts, reasons bitmask)
         self.error = None
-        self._nvml = None
-        self._h = None
+        self.ok = False
         self._thread = None
         self._stop = threading.Event()
         self._active = False
 
     def start(self):
+        import ctypes
         try:
-            import pynvml
-            pynvml.nvmlInit()
-            self._nvml = pynvml
-            self._h = pynvml.nvmlDeviceGetHandleByIndex(self.index)
-            self._max = float(pynvml.nvmlDeviceGetMaxClockInfo(self._h, pynvml.NVML_CLOCK_SM))
-        except Exception as e:  # NVML missing or refused: the caller falls back
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                raise RuntimeError("nvmlInit_v2 failed")
+            h = ctypes.c_void_p()
+            if lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.index), ctypes.byref(h)):
+                raise RuntimeError("nvmlDeviceGetHandleByIndex_v2 failed")
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)):
+                raise RuntimeError("nvmlDeviceGetMaxClockInfo failed")
+            self._lib, self._h, self._max = lib, h, float(mx.value)
+            self._reasons = (getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                             or lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+        except Exception as e:  # no NVML: the caller falls back to nvidia-smi
             self.error = f"{type(e).__name__}: {e}"
-            self._nvml = None
             return self
+        self.ok = True
         self._thread = threading.Thread(target=self._loop, daemon=True)
         self._thread.start()
         return self
 
     def _loop(self):
-        n = self._nvml
+        import ctypes
+        clk, mw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
         while not self._stop.is_set():
             if self._active:
-                try:
-                    self.rows.append((
-                        float(n.nvmlDeviceGetClockInfo(self._h, n.NVML_CLOCK_SM)), self._max,
-                        n.nvmlDeviceGetPowerUsage(self._h) / 1000.0,
-                        int(n.nvmlDeviceGetCurrentClocksEventReasons(self._h))))
-                except Exception as e:
-                    self.error = f"{type(e).__name__}: {e}"
+                if (self._lib.nvmlDeviceGetClockInfo(self._h, self.NVML_CLOCK_SM, ctypes.byref(clk))
+                        == 0 and self._lib.nvmlDeviceGetPowerUsage(self._h, ctypes.byref(mw)) == 0
+                        and self._reasons(self._h, ctypes.byref(rs)) == 0):
+                    self.rows.append((float(clk.value), self._max, mw.value / 1000.0, rs.value))
             time.sleep(self.period_s)
 
     def __enter__(self):
@@ -229,29 +242,28 @@ class NvmlClockSampler:
             self._thread.join(timeout=2)
 
     def summary(self):
-        n = self._nvml
-        bits = {} if n is None else {
-            "hw_slowdown": n.nvmlClocksEventReasonHwSlowdown,
-            "hw_thermal_slowdown": n.nvmlClocksEventReasonHwThermalSlowdown,
-            "sw_thermal_slowdown": n.nvmlClocksEventReasonSwThermalSlowdown,
-            "sw_power_cap": n.nvmlClocksEventReasonSwPowerCap,
-            "hw_power_brake_slowdown": n.nvmlClocksEventReasonHwPowerBrakeSlowdown}
-        reasons = sorted({name for *_, r in self.rows for name, b in bits.items() if r & b})
+        reasons = sorted({name for *_, r in self.rows for name, b in self.REASONS.items()
+                          if r & b})
         mhz = [r[0] for r in self.rows]
         out = {"sm_mhz": statistics.median(mhz) if mhz else None,
                "sm_max_mhz": max(r[1] for r in self.rows) if mhz else None,
                "power_w_max": max(r[2] for r in self.rows) if mhz else None,
                "reasons": reasons, "samples": len(mhz),
-               "source": f"NVML, every {self.period_s * 1e3:g} ms"}
+               "source": f"NVML (libnvidia-ml), every {self.period_s * 1e3:g} ms"}
         if self.error:
             out["error"] = self.error
         return out
 
 
 def clock_sampler(device_index: int):
-    """NVML sampler when NVML answers, else the nvidia-smi one."""
+    """NVML sampler when NVML answers, else the nvidia-smi one (whose summary
+    then names NVML's error)."""
     s = NvmlClockSampler(device_index).start()
-    return s if s._nvml is not None else ClockSampler(device_index).start()
+    if s.ok:
+        return s
+    fallback = ClockSampler(device_index).start()
+    fallback.nvml_error = s.error
+    return fallback
 
 
 # ------------------------------------------------------------ CPU oracle --

@@ -86,6 +86,10 @@ WORKLOADS = {
     # head dimension 256 (the same FLOPs as the d = 128 prefill shape: half the heads)
     "d256_b2h16s8192_causal": Workload("d256_b2h16s8192_causal", 2, 16, 16, 8192, 8192, 256,
                                        True, seed=1007),
+    # head dimension 64 at long context (twice the heads of the d = 128 prefill shape,
+    # the same FLOPs): the d = 64 instantiation of the forward kernel
+    "d64_b2h64s8192_causal": Workload("d64_b2h64s8192_causal", 2, 64, 64, 8192, 8192, 64, True,
+                                      seed=1008),
     # fp16 variant of the long-context prefill shape (the FA3 page benchmarks FP16)
     "f16_b2h32s8192d128_causal": Workload("f16_b2h32s8192d128_causal", 2, 32, 32, 8192, 8192, 128,
                                           True, dtype="f16", seed=1005),

@@ -138,7 +138,7 @@ def test_b4h16s2048_causal_full_compare(oracle_mod):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("name", ["b2h32s8192d128_causal", "b2h32s8192d128",
-                                  "gqa_b1hq32hkv8s16384d128_causal"])
+                                  "gqa_b1hq32hkv8s16384d128_causal", "d64_b2h64s8192_causal"])
 def test_full_size_workloads_every_tile(oracle_mod, name):
     """The long-context workloads in the benchmark's launch configuration
     (pair-order schedule): the first, the last and one random row of every
