@@ -117,6 +117,12 @@ int launch(const void* q, const void* k, const void* v, const float* qs, const f
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_ALLOC) !=
         cudaSuccess)
       return ATTN_ERR_CUDA;
+    // A kernel that moves registers between its warpgroups (setmaxnreg) must
+    // be launched with enough of them for the new split, or the softmax
+    // warps' increase would wait forever: refuse to launch instead.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return ATTN_ERR_CUDA;
+    if (static_cast<long long>(fa.numRegs) * C::THREADS < C::REGS_NEEDED) return ATTN_ERR_CUDA;
     di->attr_done.fetch_or(attr_bit, std::memory_order_acq_rel);
   }
   CUtensorMap tq, tk, tv;

@@ -123,6 +123,17 @@ struct Cfg {
   static constexpr float RESCALE = RESCALE_LOG2;  // stale-max threshold, log2 units
   static_assert(P_COLS <= BN, "P must fit in the S columns");
   static constexpr int THREADS = FP8 ? NUM_THREADS_FP8 : NUM_THREADS;
+  // E4M3 inputs: warps 8-11 (MMA, TMA, V widening) form a whole warpgroup,
+  // which gives up registers at start-up so the softmax warpgroups can use
+  // more (the E4M3 softmax, with its per-block scales, does not fit in the
+  // 168 a thread the 384-thread launch gets). 256 * REGS_SOFTMAX + 128 *
+  // REGS_OTHER must not exceed the registers the block was launched with
+  // (384 * 168); the host checks it before launching, since an increase that
+  // cannot be met would wait forever.
+  static constexpr bool REBALANCE = FP8;
+  static constexpr int REGS_SOFTMAX = 192;
+  static constexpr int REGS_OTHER = 104;
+  static constexpr int REGS_NEEDED = REBALANCE ? 256 * REGS_SOFTMAX + 128 * REGS_OTHER : 0;
   static constexpr int V16_TILE_BYTES = BN * D * 2;  // FP8: a widened V tile
   // operand format: kind::f8f6f4 0 = e4m3; kind::f16 0 = f16, 1 = bf16
   static constexpr uint32_t AB_FMT = (FP8 || F16) ? 0u : 1u;
@@ -429,6 +440,9 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = ctl->tmem_base;
 
+  if (warp >= 8) {
+  // ===================================== warps 8+ (MMA, TMA, V widening)
+  if constexpr (C::REBALANCE) setmaxnreg_dec<C::REGS_OTHER>();
   if (warp == WARP_LOAD) {
     // ------------------------------------------------------- TMA producer
     if (lane == 0) {
@@ -613,8 +627,10 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
       }
       it += 2 * U.nmax;
     }
+  }
   } else {
-    // ------------------------------------------------------------- softmax
+    // ========================================= softmax warpgroups 0 and 1
+    if constexpr (C::REBALANCE) setmaxnreg_inc<C::REGS_SOFTMAX>();
     const int t = warp >> 2;           // Q tile handled by this warpgroup
     const int quad = warp & 3;         // TMEM lane quadrant of this warp
     const int rloc = quad * 32 + lane; // row within the tile == TMEM lane
