@@ -673,6 +673,26 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
       }
 
       for (int j = 0; j < n; ++j) {
+        // per-column-half exponent scales. FP8: the first and second 64 keys
+        // of the tile are two scale blocks of K and of V; e_* = log2 of the
+        // factor p is multiplied by before it is rounded to fp16 (V block
+        // scale / largest V scale of the head, <= 1), inv_* = 1 / that factor.
+        // They depend only on the tile, so they are formed before the wait
+        // for S, off the path from S to P.
+        float c_lo = cq, c_hi = cq;
+        float e_lo = 0.f, e_hi = 0.f;
+        float inv_lo = 1.f, inv_hi = 1.f;
+        if (FP8 && ks_row != nullptr) {
+          const int kb0 = 2 * (U.j0 + j), kb1 = kb0 + 1;
+          const float vs0 = vs_row[kb0];
+          const float vs1 = kb1 < nblk_k ? vs_row[kb1] : v_ref;
+          c_lo = cq * ks_row[kb0];
+          c_hi = cq * (kb1 < nblk_k ? ks_row[kb1] : 1.f);
+          e_lo = __log2f(vs0 / v_ref);
+          e_hi = __log2f(vs1 / v_ref);
+          inv_lo = v_ref / vs0;
+          inv_hi = v_ref / vs1;
+        }
         bool w = wait_bounded(BAR_S_FULL + 8 * t, sc & 1u, ctl, P);
         ++sc;
         if (!__all_sync(0xffffffffu, w)) { ok = false; break; }
@@ -707,24 +727,6 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
 #pragma unroll
           for (int c = 0; c < BN; ++c)
             if (c >= vis) s[c] = -INFINITY;
-        }
-        // per-column-half exponent scales. FP8: the first and second 64 keys
-        // of the tile are two scale blocks of K and of V; e_* = log2 of the
-        // factor p is multiplied by before it is rounded to fp16 (V block
-        // scale / largest V scale of the head, <= 1), inv_* = 1 / that factor.
-        float c_lo = cq, c_hi = cq;
-        float e_lo = 0.f, e_hi = 0.f;
-        float inv_lo = 1.f, inv_hi = 1.f;
-        if (FP8 && ks_row != nullptr) {
-          const int kb0 = 2 * (U.j0 + j), kb1 = kb0 + 1;
-          const float vs0 = vs_row[kb0];
-          const float vs1 = kb1 < nblk_k ? vs_row[kb1] : v_ref;
-          c_lo = cq * ks_row[kb0];
-          c_hi = cq * (kb1 < nblk_k ? ks_row[kb1] : 1.f);
-          e_lo = __log2f(vs0 / v_ref);
-          e_hi = __log2f(vs1 / v_ref);
-          inv_lo = v_ref / vs0;
-          inv_hi = v_ref / vs1;
         }
         // row max of each 64-key half (raw scores; the exponent scale of a
         // half is positive, so it commutes with the max)
