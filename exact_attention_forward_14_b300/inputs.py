@@ -66,6 +66,9 @@ WORKLOADS = {
                                                 16384, 16384, 128, True, seed=1003),
     "fp8_b4h16s4096d128": Workload("fp8_b4h16s4096d128", 4, 16, 16, 4096, 4096, 128, False,
                                    dtype="e4m3", outlier_frac=0.001, seed=1004),
+    # the FP8 workload's shape in bf16 (N(0, 1), no outliers), to compare the two input
+    # types on one shape
+    "b4h16s4096d128": Workload("b4h16s4096d128", 4, 16, 16, 4096, 4096, 128, False, seed=1004),
     # long key side, short query side (the last 256 rows of a 64K context, GQA):
     # 32 work items alone leave most SMs idle; the split-KV form fills them
     "longkv_b1hq32hkv8sq256sk65536d128": Workload("longkv_b1hq32hkv8sq256sk65536d128", 1, 32, 8,
