@@ -158,7 +158,16 @@ struct Cfg {
   // warps, K slots from the MMA thread)
   static_assert(NSLOT % 2 == 0, "K/V slots alternate");
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;
+  // 16-bit inputs: each softmax warp writes its 32 output rows through a
+  // 2 KB staging area (32 rows x 64 bytes, one 32-column quarter of O at a
+  // time), so that each global store instruction writes 64 contiguous bytes
+  // of 8 rows instead of 16 bytes of 32 rows. (E4M3 inputs: no room left;
+  // d = 64: the staging code makes the softmax spill at its register cap.
+  // Those rows are stored directly.)
+  static constexpr bool STAGE_O = !FP8 && D >= 128;
+  static constexpr int OSTAGE_WARP_BYTES = 32 * 64;
+  static constexpr int OFF_OSTAGE = (OFF_MISC + 16 + 127) / 128 * 128;
+  static constexpr int SMEM_BYTES = OFF_OSTAGE + (STAGE_O ? 8 * OSTAGE_WARP_BYTES : 0) + 1024;
   // Launch with the whole opt-in budget (one CTA per SM either way), so a
   // descriptor stepping past its tile still reads inside this CTA's window.
   static constexpr int SMEM_ALLOC = 227 * 1024;
@@ -526,11 +535,19 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
                                    half, acc);
     };
 
+    // The next unit is worked out while this one's products run, so that
+    // the step from one unit's last P V to the next unit's first S is only
+    // waits and issues.
+    Unit Un;
+    int stn = cta_unit(0, P, Un);
     for (int i = 0; ok; ++i) {
-      Unit U;
-      const int st = cta_unit(i, P, U);
+      const Unit U = Un;
+      const int st = stn;
       if (st == 0) break;
-      if (st == 1 || U.nmax == 0) continue;
+      if (st == 1 || U.nmax == 0) {
+        stn = cta_unit(i + 1, P, Un);
+        continue;
+      }
       if (!wait_w(BAR_Q_FULL, qit & 1u)) { ok = false; break; }
       tc_fence_after();
       {
@@ -546,6 +563,7 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
         tc_commit_w(BAR_KV_EMPTY + 8 * slot);
         if (U.nmax == 1) tc_commit_w(BAR_Q_EMPTY);
       }
+      stn = cta_unit(i + 1, P, Un);
       for (int j = 0; j < U.nmax; ++j) {
         const uint32_t itv = it + 2 * j + 1, vslot = itv % C::NSLOT;
         const uint32_t itk = itv + 1, kslot = itk % C::NSLOT;
@@ -857,20 +875,66 @@ __global__ void __launch_bounds__(Cfg<D, FP8, F16>::THREADS, 1)
         tc_fence_after();
         // FP8: O holds sum p * (V block scale / v_ref) * code
         const float inv = l_run > 0.f ? v_ref / l_run : 0.f;
+        if constexpr (C::STAGE_O) {
+          // Per 32-column quarter: this thread's 64 bytes of its row go to
+          // row `lane` of the warp's staging area (64-byte rows), 16-byte
+          // chunk c at position c ^ ((row >> 1) & 3), so that every 8 lanes
+          // of a shared-memory access cover all 32 banks; then store k
+          // writes rows 8k .. 8k + 7 of the warp, 4 lanes per row, 64
+          // contiguous bytes each.
+          // (the staging addresses are formed here, not hoisted out of the
+          // unit loop, where they would hold registers the softmax needs)
+          uint32_t stg = sbase + C::OFF_OSTAGE + warp * C::OSTAGE_WARP_BYTES;
+          int ln = lane, sq = P.Sq, hqn = P.Hq;
+          asm volatile("" : "+r"(stg), "+r"(ln), "+r"(sq), "+r"(hqn));
+          const int c4 = ln & 3;
+          const int rr0 = ln >> 2;  // first row this lane stores
+          const int rows_left = sq - (tile_row0 + quad * 32 + rr0);
+          const size_t ostride = static_cast<size_t>(hqn) * D;  // elements between rows
+          uint16_t* odst = P.o + ((static_cast<size_t>(U.b) * sq + tile_row0 + quad * 32 + rr0) * hqn +
+                                  U.hq) * static_cast<size_t>(D) + 8 * c4;
+#pragma unroll 1
+          for (int qq = 0; qq < D / 32; ++qq) {
+            uint32_t r[32];
+            tmem_ld32(t_lane + col_o + 32 * qq, r);
 #pragma unroll
-        for (int i = 0; i < D / 32; ++i) {
-          uint32_t r[32];
-          tmem_ld32(t_lane + col_o + 32 * i, r);
-          uint32_t pk[16];
+            for (int c = 0; c < 4; ++c) {
+              uint32_t pk[4];
 #pragma unroll
-          for (int c = 0; c < 16; ++c)
-            pk[c] = F16 ? pack_f16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv)
-                        : pack_bf16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv);
-          if (row_ok) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
+              for (int e = 0; e < 4; ++e) {
+                const float a = __uint_as_float(r[8 * c + 2 * e]) * inv;
+                const float b = __uint_as_float(r[8 * c + 2 * e + 1]) * inv;
+                pk[e] = F16 ? pack_f16x2(a, b) : pack_bf16x2(a, b);
+              }
+              sts128(stg + ln * 64 + ((c ^ ((ln >> 1) & 3)) << 4),
+                     make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            }
+            __syncwarp();
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-              dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            for (int k = 0; k < 4; ++k) {
+              const int rr = 8 * k + rr0;
+              const uint4 v = lds128(stg + rr * 64 + ((c4 ^ ((rr >> 1) & 3)) << 4));
+              if (8 * k < rows_left)
+                *reinterpret_cast<uint4*>(odst + 8 * k * ostride + 32 * qq) = v;
+            }
+            __syncwarp();  // the next quarter overwrites the staging area
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 32; ++i) {
+            uint32_t r[32];
+            tmem_ld32(t_lane + col_o + 32 * i, r);
+            uint32_t pk[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c)
+              pk[c] = F16 ? pack_f16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv)
+                          : pack_bf16x2(__uint_as_float(r[2 * c]) * inv, __uint_as_float(r[2 * c + 1]) * inv);
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + 32 * i);
+#pragma unroll
+              for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
           }
         }
         if (row_ok) P.lse[lse_idx] = l_run > 0.f ? (m_run + log2f(l_run)) * LN2 : -INFINITY;
