@@ -20,10 +20,8 @@
 //
 // CTA organisation (one persistent CTA per SM, 320 threads):
 //   warps 0-3  softmax for Q tile 0 (thread = one query row = one TMEM lane)
-//   warps 4-7  softmax for Q tile 1 (ping-pong partner of tile 0); each
-//              softmax warpgroup also writes its tile's O and LSE
-//   warp  8    MMA issuer (the whole warp runs the loop; one lane chosen by
-//              elect.sync issues each instruction) and TMEM owner
+//   warps 4-7  softmax for Q tile 1 (ping-pong partner of tile 0)
+//   warp  8    MMA issuer (lane 0) and TMEM owner
 //   warp  9    TMA producer (lane 0)
 //   warps 10-11 (E4M3 inputs only, 384 threads) widen each staged E4M3 V
 //              tile to fp16 in one of two shared-memory buffers: S = Q K^T
