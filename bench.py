@@ -543,6 +543,46 @@ def e2e_pipelined(args, host_in, bufs, step, dev, dist, world, flops):
             "pipelined": "3 streams, 2 buffer sets: copies overlap neighbouring steps' compute"}
 
 
+def quant_rate(reps: int = 20):
+    """Rate of the FP8 block quantiser (attn_quantize_fp8_e4m3, outside the
+    attention's timed region) on one operand of the FP8 workload: fp32
+    [4, 4096, 16, 128] -> E4M3 codes + per-block scales. Each call is timed
+    alone with CUDA events after a write of twice the L2 (L2-cold); prints one
+    JSON line with the median and the HBM rate its bytes imply, against the
+    measured copy bandwidth."""
+    import torch
+    import exact_attention_forward_14_b300 as ea
+    from exact_attention_forward_14_b300 import inputs
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    w = inputs.WORKLOADS["fp8_b4h16s4096d128"]
+    x = inputs.draw_workload_f32(w)[0].to(dev)
+    for _ in range(5):
+        ea.quantize_fp8(x)
+    torch.cuda.synchronize(dev)
+    flush = torch.empty(2 * 126 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    times = []
+    clocks = clock_sampler(0)
+    with clocks:
+        for r in range(reps):
+            flush.fill_(float(r))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            codes, scales = ea.quantize_fp8(x)
+            e1.record()
+            torch.cuda.synchronize(dev)
+            times.append(e0.elapsed_time(e1))
+    ms = statistics.median(times)
+    nbytes = x.numel() * 4 + codes.numel() + scales.numel() * 4
+    peaks, src = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({"kernel": "quantize_fp8_kernel", "shape": list(x.shape), "us_median": ms * 1e3,
+                      "bytes": nbytes, "hbm_gbs": gbs, "peak_gbs": peaks["hbm_gbs"], "peak_source": src,
+                      "frac": gbs / peaks["hbm_gbs"], "l2": "a buffer of twice the L2 written before each call",
+                      "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def gemm_peaks(n: int = 8192, reps: int = 40):
     """Library GEMM rates on this GPU at n x n x n, as context for the FP8
     roofline: cuBLASLt E4M3 x E4M3 -> bf16 (torch._scaled_mm, unit tensor
@@ -893,6 +933,8 @@ def main(argv=None):
                     help="skip the CPU oracle timing (e.g. under a profiler)")
     ap.add_argument("--gemm-peaks", action="store_true",
                     help="only time library bf16 and FP8 GEMMs (8192^3) and exit")
+    ap.add_argument("--quant-rate", action="store_true",
+                    help="only time the FP8 block quantiser on one FP8-workload operand and exit")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="--impl reference: seconds of oracle work over all steps (bounded sample)")
     args = ap.parse_args(argv)
@@ -901,6 +943,8 @@ def main(argv=None):
         return launch_ranks(args.gpus, sys.argv[1:] if argv is None else list(argv))
     if args.gemm_peaks:
         return gemm_peaks()
+    if args.quant_rate:
+        return quant_rate()
     from exact_attention_forward_14_b300 import inputs
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":

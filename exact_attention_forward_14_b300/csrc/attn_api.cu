@@ -566,9 +566,13 @@ int attn_quantize_fp8_e4m3(const float* x, uint8_t* codes, float* scale, int B, 
   const int nblk = (S + attnb3::FP8_BLOCK - 1) / attnb3::FP8_BLOCK;
   const long long ctas = static_cast<long long>(B) * H * nblk;
   if (ctas > 0x7fffffffLL) return ATTN_ERR_INVALID_ARG;
-  attnb3::quantize_fp8_kernel<<<static_cast<unsigned>(ctas), attnb3::QUANT_THREADS, 0,
-                                reinterpret_cast<cudaStream_t>(stream)>>>(x, codes, scale, S, H,
-                                                                          d, nblk);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (d == 128)
+    attnb3::quantize_fp8_kernel<128><<<static_cast<unsigned>(ctas), attnb3::QUANT_THREADS, 0, st>>>(
+        x, codes, scale, S, H, nblk);
+  else
+    attnb3::quantize_fp8_kernel<64><<<static_cast<unsigned>(ctas), attnb3::QUANT_THREADS, 0, st>>>(
+        x, codes, scale, S, H, nblk);
   return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
