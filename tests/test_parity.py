@@ -174,10 +174,61 @@ def test_pair_order_schedule_medium_shape_full(oracle_mod, causal):
            assert_lse_close(lse, lse_ref), Hq * S)
 
 
+# ------------------------------------------------- d = 64, medium shapes --
+# (B, Hq, Hkv, Sq, Sk, d, causal): several 256-row units per head, Q and K/V
+# tails inside a unit, causal Sq > Sk (rows with no visible key) and Sq < Sk,
+# GQA, and one head long enough for the causal tile skip to matter.
+D64_SHAPES = [
+    (1, 2, 2, 1100, 1100, 64, True),
+    (2, 3, 1, 700, 1000, 64, False),
+    (1, 2, 2, 1000, 700, 64, True),
+    (1, 2, 2, 600, 1500, 64, True),
+    (1, 1, 1, 2048, 2048, 64, True),
+]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", D64_SHAPES, ids=lambda s: "d64_b{}hq{}hkv{}sq{}sk{}{}".format(
+    *s[:5], "c" if s[6] else ""))
+def test_d64_medium_shapes_full_compare(oracle_mod, shape):
+    torch = require_gpu()
+    B, Hq, Hkv, Sq, Sk, d, causal = shape
+    q, k, v = inputs.draw_qkv_bf16(B, Hq, Hkv, Sq, Sk, d, seed=sum(shape) + 41)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_bf16(torch, q, k, v, causal, scale)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
+                                         inputs.bf16_bits(v), causal, scale)
+    st = assert_o_close(o, o_ref)
+    record("d64 units b{}hq{}hkv{}sq{}sk{}{}".format(*shape[:5], "c" if causal else ""), "bf16",
+           st, assert_lse_close(lse, lse_ref), B * Hq * Sq)
+
+
+@pytest.mark.gpu
+def test_d64_pair_order_schedule_full(oracle_mod):
+    """d = 64 with at least 4 work items per SM, so the host picks the pair
+    order; S = 1100 gives an odd number of 256-row levels (5), so one item
+    per head runs the middle level alone. Compared in full."""
+    torch = require_gpu()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    Hq, S, d = 2 * sms, 1100, 64
+    Hkv = Hq // 2
+    n_qp = -(-S // 256)
+    assert n_qp % 2 == 1 and Hq * ((n_qp + 1) // 2) >= 4 * sms
+    q, k, v = inputs.draw_qkv_bf16(1, Hq, Hkv, S, S, d, seed=1100)
+    scale = 1.0 / np.sqrt(d)
+    o, lse = run_bf16(torch, q, k, v, True, scale)
+    o_ref, lse_ref = oracle_mod.attn_fwd(inputs.bf16_bits(q), inputs.bf16_bits(k),
+                                         inputs.bf16_bits(v), True, scale)
+    st = assert_o_close(o, o_ref)
+    record(f"d64 pair order b1hq{Hq}hkv{Hkv}s{S}c (full)", "bf16", st,
+           assert_lse_close(lse, lse_ref), Hq * S)
+
+
 # ------------------------------------------------------------ fp16 inputs --
 # (B, Hq, Hkv, Sq, Sk, d, causal): d = 64 and 128, GQA, ragged tails, Sq != Sk
 SMALL_F16 = [
     (1, 2, 2, 128, 128, 128, False),
+    (1, 2, 2, 1100, 900, 64, True),
     (2, 4, 2, 300, 300, 128, True),
     (1, 2, 2, 127, 300, 64, True),
     (1, 4, 1, 600, 513, 128, False),
