@@ -46,8 +46,11 @@ DEFAULT_WORKLOAD = "b2h32s8192d128_causal"
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
 KERNEL_SOURCES = ["exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
                   "exact_attention_forward_14_b300/csrc/ptx.cuh"]
+# the backward's traffic also depends on how the host launches its kernels
+# (dK/dV and dQ side by side on split SMs), so the host file is part of it
 KERNEL_SOURCES_BWD = ["exact_attention_forward_14_b300/csrc/attn_bwd_kernel.cuh",
-                      "exact_attention_forward_14_b300/csrc/ptx.cuh"]
+                      "exact_attention_forward_14_b300/csrc/ptx.cuh",
+                      "exact_attention_forward_14_b300/csrc/attn_api.cu"]
 KERNEL_SOURCES_D256 = ["exact_attention_forward_14_b300/csrc/attn_fwd_d256.cuh",
                        "exact_attention_forward_14_b300/csrc/attn_fwd_kernel.cuh",
                        "exact_attention_forward_14_b300/csrc/ptx.cuh"]
@@ -772,6 +775,8 @@ def run_ours(args, w):
     torch.cuda.synchronize(dev)
     clocks = clock_sampler(local)
     with clocks:
+        if args.profiler_range:
+            torch.cuda.profiler.start()
         t0.record(stream)
         for i, (a, b) in enumerate(ev):
             if flush is not None:
@@ -781,6 +786,8 @@ def run_ours(args, w):
             b.record(stream)
         t1.record(stream)
         torch.cuda.synchronize(dev)
+        if args.profiler_range:
+            torch.cuda.profiler.stop()
     if dist is not None:
         dist.barrier()
     st = ea.attn_device_status(stream)
@@ -935,6 +942,10 @@ def main(argv=None):
                     help="only time library bf16 and FP8 GEMMs (8192^3) and exit")
     ap.add_argument("--quant-rate", action="store_true",
                     help="only time the FP8 block quantiser on one FP8-workload operand and exit")
+    ap.add_argument("--profiler-range", action="store_true",
+                    help="bracket the timed region with cudaProfilerStart/Stop, so that ncu "
+                         "--replay-mode app-range measures it as a whole (kernels that run "
+                         "side by side included); never for a bench value")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="--impl reference: seconds of oracle work over all steps (bounded sample)")
     args = ap.parse_args(argv)

@@ -42,6 +42,11 @@ std::atomic<unsigned long long> g_wait_limit_ns{kWaitLimitDefaultNs};
 
 unsigned long long wait_limit_ns() { return g_wait_limit_ns.load(std::memory_order_relaxed); }
 constexpr int kMaxSplits = 256;  // key ranges per split-KV call
+// Backward: share of the SMs given to the dK/dV kernel while the dQ kernel
+// runs beside it (the two kernels' times alone on all SMs were 1.51 and
+// 1.07 ms on B2 H32 S8192 d128 causal: 0.585 of the sum).
+constexpr int kBwdKvShareNum = 585;
+constexpr int kBwdKvShareDen = 1000;
 
 struct DeviceInfo {
   std::once_flag once;
@@ -49,6 +54,14 @@ struct DeviceInfo {
   int num_sms = 0;
   int* status = nullptr;
   std::atomic<uint32_t> attr_done{0};  // bit per kernel instantiation
+  // backward: a second stream for the dQ kernel, forked from and joined back
+  // into the caller's stream with two events (created on the first attn_bwd
+  // call; side == nullptr if that failed: then both kernels go on the
+  // caller's stream one after the other)
+  std::once_flag side_once;
+  cudaStream_t side = nullptr;
+  cudaEvent_t fork = nullptr, join = nullptr;
+  std::mutex side_mu;  // one fork / join sequence at a time per device
 };
 DeviceInfo g_dev[kMaxDevices];
 
@@ -360,11 +373,50 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
                                     attnb3::BWD_PREP_THREADS, 0, stream>>>(
       static_cast<const uint16_t*>(o), static_cast<const uint16_t*>(d_o), lse, ws,
       ws + rows_pad, Hq, Sq, P.Sq_pad, rows, row_warps, pad_rows);
-  const int gkv = P.kv_items < di->num_sms ? P.kv_items : di->num_sms;
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+
+  // dK/dV and dQ read the same Q, dO, K and V and do not depend on each
+  // other. They run side by side on disjoint sets of SMs, sized to their
+  // work (dK/dV: four products per (Q tile, key tile) pair, dQ: three, at
+  // slightly different efficiencies), and both deal their items head by
+  // head in the same order, so the two kernels are on the same few heads at
+  // any time and the second read of those heads' tiles comes from L2.
+  std::call_once(di->side_once, [&] {
+    cudaStream_t s = nullptr;
+    cudaEvent_t f = nullptr, j = nullptr;
+    if (cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking) == cudaSuccess &&
+        cudaEventCreateWithFlags(&f, cudaEventDisableTiming) == cudaSuccess &&
+        cudaEventCreateWithFlags(&j, cudaEventDisableTiming) == cudaSuccess) {
+      di->side = s;
+      di->fork = f;
+      di->join = j;
+    } else {
+      cudaGetLastError();  // clear the failed creation; fall back to one stream
+    }
+  });
+  const int sms = di->num_sms;
+  int share_kv = (sms * kBwdKvShareNum + kBwdKvShareDen / 2) / kBwdKvShareDen;
+  share_kv = share_kv < 1 ? 1 : (share_kv > sms - 1 ? sms - 1 : share_kv);
+  if (di->side == nullptr || sms < 2) {
+    const int gkv = P.kv_items < sms ? P.kv_items : sms;
+    kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
+    const int gq = P.q_items < sms ? P.q_items : sms;
+    kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
+    return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  const int gkv = P.kv_items < share_kv ? P.kv_items : share_kv;
+  const int gq = P.q_items < sms - share_kv ? P.q_items : sms - share_kv;
+  std::lock_guard<std::mutex> lock(di->side_mu);
+  if (cudaEventRecord(di->fork, stream) != cudaSuccess ||
+      cudaStreamWaitEvent(di->side, di->fork, 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
   kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
-  const int gq = P.q_items < di->num_sms ? P.q_items : di->num_sms;
-  kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
-  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, di->side>>>(tq, tdo, tk, tv, P);
+  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
+  if (cudaEventRecord(di->join, di->side) != cudaSuccess ||
+      cudaStreamWaitEvent(stream, di->join, 0) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  return ATTN_OK;
 }
 
 // ---- workspace for attn_fwd_splitkv_noalloc --------------------------------

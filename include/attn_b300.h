@@ -241,9 +241,16 @@ int attn_bwd_workspace_size(int B, int Hq, int Sq, size_t* workspace_bytes);
  *                return undefined
  * Other arguments as attn_fwd, with d in {64, 128}. P and dS are rounded to dtype before they
  * enter the tensor cores (fp32 accumulation); the gradients are rounded to
- * nearest in dtype. Three kernels are enqueued on `stream` (row statistics,
- * dK/dV, dQ); every output element is written exactly once, so results are
- * deterministic. Calls that share a workspace must not overlap. Errors as
+ * nearest in dtype. Three kernels run: row statistics on `stream`, then
+ * dK/dV on `stream` and dQ on a second stream of the library's, side by side
+ * on disjoint SMs (that stream waits for `stream` through an event before dQ,
+ * and `stream` waits for it after; work later on `stream` sees all three
+ * gradients, and the sequence can be captured into a CUDA graph). The first
+ * call on a device creates that stream and its two events: make it before
+ * any stream capture. If creating them fails, both kernels go on `stream`
+ * one after the other. Every output element is written exactly once, so
+ * results are deterministic and the same either way. Calls that share a
+ * workspace must not overlap. Errors as
  * attn_fwd; ATTN_ERR_INVALID_ARG for a missing or too small workspace or for
  * B * Hq * Sq_pad >= 2^31, ATTN_ERR_MISALIGNED for a workspace or gradient
  * pointer not 16-byte aligned, ATTN_ERR_UNSUPPORTED for d = 256 or E4M3.
