@@ -102,6 +102,35 @@ def test_backward_is_deterministic():
 
 
 @pytest.mark.gpu
+def test_backward_results_are_complete_on_the_callers_stream():
+    """dK/dV and dQ run side by side, dQ on a second stream of the library's
+    that is forked from the caller's stream and joined back into it. Work
+    enqueued on the caller's stream right after the call, with no host
+    synchronisation in between, must see all three gradients complete: the
+    outputs start as NaN, the call is queued behind a long fill so that it
+    runs while the host has already enqueued the copies, and the copies must
+    equal a separately synchronised call bit for bit."""
+    torch = require_gpu()
+    B, Hq, Hkv, S, d = 1, 16, 4, 4096, 128
+    q, k, v = (t.cuda() for t in inputs.draw_qkv_bf16(B, Hq, Hkv, S, S, d, seed=17))
+    do = inputs.draw_grad_out(B, S, Hq, d, 17).cuda()
+    o, lse = ea.forward(q, k, v, causal=True)
+    ref = ea.backward(q, k, v, o, lse, do, causal=True)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        out = tuple(torch.full_like(t, float("nan")) for t in ref)
+        busy = torch.empty(1 << 30, dtype=torch.uint8, device="cuda")
+        busy.fill_(1)
+        g = ea.backward(q, k, v, o, lse, do, causal=True, out=out, stream=side)
+        copies = tuple(t.clone() for t in g)
+    torch.cuda.synchronize()
+    assert ea.attn_device_status() == ea.ATTN_OK
+    for name, got, want in zip(("dq", "dk", "dv"), copies, ref):
+        assert torch.equal(got, want), name
+
+
+@pytest.mark.gpu
 def test_gqa_equals_mha_on_repeated_kv_heads():
     """Property at any size: with each KV head repeated for its query heads,
     MHA's dK / dV summed over each group equal the GQA gradients (up to the
