@@ -390,8 +390,11 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
       di->side = s;
       di->fork = f;
       di->join = j;
-    } else {
-      cudaGetLastError();  // clear the failed creation; fall back to one stream
+    } else {  // fall back to one stream; release whatever was created
+      if (j != nullptr) cudaEventDestroy(j);
+      if (f != nullptr) cudaEventDestroy(f);
+      if (s != nullptr) cudaStreamDestroy(s);
+      cudaGetLastError();
     }
   });
   const int sms = di->num_sms;
@@ -412,11 +415,12 @@ int launch_bwd(const void* q, const void* k, const void* v, const void* o, const
     return ATTN_ERR_CUDA;
   kkv<<<gkv, attnb3::BWD_THREADS, C::SMEM_ALLOC, stream>>>(tq, tdo, tk, tv, P);
   kq<<<gq, attnb3::BWD_THREADS, C::SMEM_ALLOC, di->side>>>(tq, tdo, tk, tv, P);
-  if (cudaGetLastError() != cudaSuccess) return ATTN_ERR_CUDA;
-  if (cudaEventRecord(di->join, di->side) != cudaSuccess ||
-      cudaStreamWaitEvent(stream, di->join, 0) != cudaSuccess)
-    return ATTN_ERR_CUDA;
-  return ATTN_OK;
+  const cudaError_t launched = cudaGetLastError();
+  // join even after a failed launch, so that the caller's stream never runs
+  // ahead of work already enqueued on the second one
+  const bool joined = cudaEventRecord(di->join, di->side) == cudaSuccess &&
+                      cudaStreamWaitEvent(stream, di->join, 0) == cudaSuccess;
+  return (launched == cudaSuccess && joined) ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 // ---- workspace for attn_fwd_splitkv_noalloc --------------------------------
