@@ -25,10 +25,11 @@
  * Ownership and execution: every pointer is a DEVICE pointer owned by the
  * caller. The library allocates no device memory, holds no per-call workspace
  * and keeps no state between calls except a cached driver entry point, the
- * per-device kernel attributes and one device status word (below). Work is
- * enqueued on `stream` (0 = legacy default stream) and the call returns
- * without synchronising; device-side failures surface through
- * attn_device_status(). All entry points are thread-safe.
+ * per-device kernel attributes, one device status word (below) and, once
+ * attn_bwd has run on a device, one stream and two events of its own there
+ * (see attn_bwd). Work is enqueued on `stream` (0 = legacy default stream)
+ * and the call returns without synchronising; device-side failures surface
+ * through attn_device_status(). All entry points are thread-safe.
  *
  * Error behaviour: argument checks run on the host before anything is
  * enqueued; a failed check returns its code and launches nothing.
