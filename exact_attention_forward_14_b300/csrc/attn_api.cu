@@ -210,7 +210,7 @@ int launch_d256(const void* q, const void* k, const void* v, void* o, float* lse
   if (!encode_bshd(&tq, q, false, B, Sq, Hq, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::BM, F16) ||
       !encode_bshd(&tk, k, false, B, Sk, Hkv, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::WIDE_BN,
                    F16) ||
-      !encode_bshd(&tv, v, false, B, Sk, Hkv, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::WIDE_BN,
+      !encode_bshd(&tv, v, false, B, Sk, Hkv, attnb3::WIDE_D, C::CHUNK_ELEMS, attnb3::WIDE_VROWS,
                    F16))
     return ATTN_ERR_CUDA;
   FwdParams P{};
