@@ -8,7 +8,7 @@ import exact_attention_forward_14_b300 as ea
 from exact_attention_forward_14_b300 import inputs
 from tests.helpers import assert_lse_close, assert_o_close, require_gpu
 
-# (B, Hq, Hkv, Sq, Sk, causal): several 64-key tiles, ragged tails, GQA,
+# (B, Hq, Hkv, Sq, Sk, causal): several 128-key steps, ragged tails, GQA,
 # Sq != Sk, fully masked rows (causal with Sq > Sk), a single row / key.
 SMALL = [
     (1, 1, 1, 1, 1, False),
@@ -43,9 +43,9 @@ def test_d256_small_full_compare(oracle_mod, shape, dtype):
 @pytest.mark.gpu
 def test_d256_rescaling(oracle_mod):
     """Scores rising along the keys, so the running max is raised and O
-    rescaled on later tiles (the rescale waits for the previous P V). At
-    scale 1/48 the 64-key tiles see 231 (row, tile) rescales after the first
-    tile. Steeper scales (1/16, 1/32) put a few elements past the bf16
+    rescaled on later steps (the rescale waits for the previous P V). At
+    scale 1/48 the 128-key steps see 131 (row, step) rescales after the first
+    step. Steeper scales (1/16, 1/32) put a few elements past the bf16
     tolerance in any implementation of the method: P is rounded to bf16 at
     up to 2^8 under the stale max, and a numpy emulation of exactly that
     arithmetic reproduces the kernel's error there element for element."""
